@@ -1,0 +1,421 @@
+// C ABI of the verification library: argument checks, launch configuration, launches.
+// The declarations and their contracts are in include/spec_verify.h.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "../../include/spec_verify.h"
+#include "spec_internal.h"
+
+namespace sv {
+const void* row_kernel_bf16(bool greedy, int nt);
+const void* row_kernel_f32(bool greedy, int nt);
+}  // namespace sv
+
+namespace {
+
+using sv::BudgetParams;
+using sv::RowParams;
+using sv::UnitRec;
+
+constexpr long long kDefaultWaitLimit = 1ll << 22;
+std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
+
+constexpr size_t kAlign = 256;
+constexpr int kMaxV = 262144;
+constexpr int kBudgetMaxKeys = 8192;
+constexpr size_t kRingBudgetSmall = 100 * 1024;   // per CTA when two CTAs share an SM
+constexpr size_t kRingBudgetLarge = 200 * 1024;   // per CTA when one CTA fills an SM
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace: [status word | pad to 256] [per-row records, B * (K+1) * 32 bytes]
+struct WsLayout {
+  size_t status, recs, total;
+};
+WsLayout ws_layout(int B, int K) {
+  WsLayout L;
+  L.status = 0;
+  L.recs = kAlign;
+  L.total = L.recs + align_up(static_cast<size_t>(B > 0 ? B : 1) * (K + 1) * sizeof(UnitRec), kAlign);
+  return L;
+}
+
+// Test and tuning hooks: the last row-kernel plan, and optional overrides (0 = automatic).
+std::atomic<int> g_force_nt{0}, g_force_cluster{0}, g_force_nstage{0};
+int g_last_plan[8] = {0};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// One-time per (device, kernel) attribute setup and a cache of the cluster occupancy.
+std::mutex g_mu;
+std::map<std::tuple<int, const void*>, bool> g_attr_done;
+std::map<std::tuple<int, const void*, int, size_t>, int> g_occ;
+
+cudaError_t prepare_kernel(int dev, const void* fn) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto key = std::make_tuple(dev, fn);
+  if (g_attr_done.count(key)) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kRingBudgetLarge + 4096));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  g_attr_done[key] = true;
+  return cudaSuccess;
+}
+
+cudaError_t max_clusters(int dev, const void* fn, int nt, int cluster, size_t smem, int* out) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_occ.find(std::make_tuple(dev, fn, cluster, smem));
+    if (it != g_occ.end()) {
+      *out = it->second;
+      return cudaSuccess;
+    }
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(cluster, 1, 1);
+  cfg.blockDim = dim3(nt, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  cudaError_t e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_occ[std::make_tuple(dev, fn, cluster, smem)] = n;
+  *out = n;
+  return cudaSuccess;
+}
+
+struct RowPlan {
+  const void* fn;
+  int nt, cluster, nclusters;
+  size_t smem;
+  RowParams p;
+};
+
+// Chooses threads per CTA, cluster size, slice and staging depth for a (dtype, V) pair.
+spec_status_t plan_rows(const void* target, const void* draft, int dtype, int B, int K, int V,
+                        float T, bool need_draft, bool stats_only, RowPlan* plan) {
+  const bool bf16 = dtype == SPEC_BF16;
+  const bool greedy = T == 0.f;
+  const int esz = bf16 ? 2 : 4;
+  int nt = V <= 256 * sv::kNV * sv::kChunk * sv::kMaxCluster ? 256 : 512;
+  if (g_force_nt.load()) nt = g_force_nt.load();
+  const int cap = nt * sv::kNV * sv::kChunk;
+  int cluster = (V + cap - 1) / cap;
+  if (g_force_cluster.load()) {
+    if (g_force_cluster.load() < cluster) return SPEC_ERR_UNSUPPORTED;
+    cluster = g_force_cluster.load();
+  }
+  if (cluster > sv::kMaxCluster) return SPEC_ERR_UNSUPPORTED;
+  int slice = (V + cluster - 1) / cluster;
+  slice = static_cast<int>(align_up(slice, sv::kChunk));
+  const bool tma = (static_cast<size_t>(V) * esz) % 16 == 0 && aligned16(target) &&
+                   (!need_draft || aligned16(draft));
+  const int stage_row_bytes = static_cast<int>(align_up(static_cast<size_t>(slice) * esz, 128));
+  const size_t stage_bytes = static_cast<size_t>(need_draft ? 2 : 1) * stage_row_bytes;
+  int nstage = 0;
+  if (tma) {
+    const size_t budget = nt == 256 ? kRingBudgetSmall : kRingBudgetLarge;
+    nstage = static_cast<int>(budget / stage_bytes);
+    if (nstage > 4) nstage = 4;
+    if (nstage < 1) nstage = 1;
+    if (g_force_nstage.load() > 0 && g_force_nstage.load() <= 4) nstage = g_force_nstage.load();
+  }
+  plan->fn = bf16 ? sv::row_kernel_bf16(greedy, nt) : sv::row_kernel_f32(greedy, nt);
+  plan->nt = nt;
+  plan->cluster = cluster;
+  plan->smem = tma ? static_cast<size_t>(nstage) * stage_bytes : 0;
+  RowParams& p = plan->p;
+  std::memset(&p, 0, sizeof(p));
+  p.target = target;
+  p.draft = draft;
+  p.B = B;
+  p.K = K;
+  p.V = V;
+  p.U = stats_only ? K : K + 1;
+  p.total_units = B * p.U;
+  p.slice = slice;
+  p.nstage = nstage;
+  p.stage_row_bytes = stage_row_bytes;
+  p.flags = (need_draft ? sv::F_NEED_DRAFT : 0) | (stats_only ? sv::F_STATS_ONLY : 0) |
+            (tma ? sv::F_TMA : 0);
+  p.c = greedy ? 0.f : static_cast<float>(1.4426950408889634 / static_cast<double>(T));
+  p.wait_limit = g_wait_limit.load();
+  return SPEC_OK;
+}
+
+spec_status_t launch_plan(RowPlan* plan, cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (prepare_kernel(dev, plan->fn) != cudaSuccess) return SPEC_ERR_CUDA;
+  int maxc = 0;
+  if (max_clusters(dev, plan->fn, plan->nt, plan->cluster, plan->smem, &maxc) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  if (maxc < 1) return SPEC_ERR_UNSUPPORTED;
+  const int ncl = plan->p.total_units < maxc ? plan->p.total_units : maxc;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = plan->cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(ncl * plan->cluster, 1, 1);
+  cfg.blockDim = dim3(plan->nt, 1, 1);
+  cfg.dynamicSmemBytes = plan->smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&plan->p};
+  if (cudaLaunchKernelExC(&cfg, plan->fn, args) != cudaSuccess) return SPEC_ERR_CUDA;
+  const int rec[8] = {plan->nt, plan->cluster, ncl, maxc, plan->p.slice, plan->p.nstage,
+                      static_cast<int>(plan->smem), plan->p.flags};
+  std::memcpy(g_last_plan, rec, sizeof(rec));
+  return SPEC_OK;
+}
+
+bool bad_T(float T) { return !(T >= 0.f) || std::isinf(T); }
+
+spec_status_t check_ws(void* ws, size_t ws_bytes, int B, int K) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return SPEC_ERR_WORKSPACE;
+  if (ws_bytes < ws_layout(B, K).total) return SPEC_ERR_WORKSPACE;
+  return SPEC_OK;
+}
+
+struct VerifyArgs {
+  const void* target;
+  const void* draft;
+  int dtype;
+  const int32_t* tokens;
+  const float* uniforms;
+  int B, K, V;
+  float T;
+  const int32_t* depth;
+  int budget;
+  int32_t* out_tokens;
+  int32_t* out_accepted;
+  float* out_alpha;
+  float* out_cum;
+  float* out_E;
+  int32_t* out_depth;
+  void* ws;
+  size_t ws_bytes;
+  cudaStream_t stream;
+};
+
+spec_status_t run_verify(const VerifyArgs& a) {
+  if (a.dtype != SPEC_F32 && a.dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+  if (a.B < 0 || a.K < 0 || a.V < 1 || bad_T(a.T)) return SPEC_ERR_INVALID_ARG;
+  if (a.K > sv::kMaxK || a.V > kMaxV) return SPEC_ERR_UNSUPPORTED;
+  if (a.B == 0) return SPEC_OK;
+  const bool greedy = a.T == 0.f;
+  const bool budget = a.budget >= 0;
+  if (budget && a.depth) return SPEC_ERR_INVALID_ARG;
+  if (budget && static_cast<long long>(a.B) * a.K > kBudgetMaxKeys) return SPEC_ERR_UNSUPPORTED;
+  const bool want_alpha = a.out_alpha || a.out_cum || a.out_E || budget;
+  const bool need_draft = a.K > 0 && (!greedy || want_alpha);
+  if (!a.target || !a.out_tokens || !a.out_accepted) return SPEC_ERR_INVALID_ARG;
+  if (a.K > 0 && !a.tokens) return SPEC_ERR_INVALID_ARG;
+  if (need_draft && !a.draft) return SPEC_ERR_INVALID_ARG;
+  if (!greedy && !a.uniforms) return SPEC_ERR_INVALID_ARG;
+  spec_status_t st = check_ws(a.ws, a.ws_bytes, a.B, a.K);
+  if (st != SPEC_OK) return st;
+
+  RowPlan plan;
+  st = plan_rows(a.target, a.draft, a.dtype, a.B, a.K, a.V, a.T, need_draft, false, &plan);
+  if (st != SPEC_OK) return st;
+  const WsLayout L = ws_layout(a.B, a.K);
+  uint8_t* ws = static_cast<uint8_t*>(a.ws);
+  RowParams& p = plan.p;
+  p.tokens = a.tokens;
+  p.uniforms = a.uniforms;
+  p.depth = a.depth;
+  p.out_tokens = a.out_tokens;
+  p.out_accepted = a.out_accepted;
+  p.out_alpha = a.out_alpha;
+  p.out_cum = a.out_cum;
+  p.out_E = a.out_E;
+  p.recs = reinterpret_cast<UnitRec*>(ws + L.recs);
+  p.status = reinterpret_cast<int32_t*>(ws + L.status);
+  st = launch_plan(&plan, a.stream);
+  if (st != SPEC_OK) return st;
+
+  BudgetParams bp;
+  std::memset(&bp, 0, sizeof(bp));
+  bp.alpha_in = nullptr;
+  bp.recs = p.recs;
+  bp.U = p.U;
+  bp.B = a.B;
+  bp.K = a.K;
+  bp.V = a.V;
+  bp.N = a.budget;
+  bp.greedy = greedy;
+  bp.do_cut = 1;
+  bp.stats_only = 0;
+  bp.tokens = a.tokens;
+  bp.uniforms = a.uniforms;
+  bp.out_depth = a.out_depth;
+  bp.out_tokens = a.out_tokens;
+  bp.out_accepted = a.out_accepted;
+  bp.out_alpha = a.out_alpha;
+  bp.out_cum = a.out_cum;
+  bp.out_E = a.out_E;
+  bp.status = p.status;
+  const cudaError_t e = budget ? sv::launch_budget_cut(bp, a.stream) : sv::launch_cut(bp, a.depth, a.stream);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_version(void) { return 100; }
+
+const char* spec_error_string(int status) {
+  switch (status) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_INVALID_ARG: return "invalid argument";
+    case SPEC_ERR_UNSUPPORTED: return "unsupported size";
+    case SPEC_ERR_CUDA: return "CUDA launch or runtime error";
+    case SPEC_ERR_DEVICE_TIMEOUT: return "a bounded device wait ran out";
+    case SPEC_ERR_TOKEN_RANGE: return "draft token id outside [0, V)";
+    case SPEC_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
+    default: return "unknown status";
+  }
+}
+
+size_t spec_workspace_bytes(int B, int K, int V, int dtype) {
+  (void)V;
+  (void)dtype;
+  if (B < 0 || K < 0) return 0;
+  return ws_layout(B, K).total;
+}
+
+spec_status_t spec_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0) return SPEC_ERR_WORKSPACE;
+  return cudaMemsetAsync(workspace, 0, ws_bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SPEC_OK
+             : SPEC_ERR_CUDA;
+}
+
+spec_status_t spec_get_status(void* workspace, void* stream, int32_t* out_status) {
+  if (!workspace || !out_status) return SPEC_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t h = 0;
+  if (cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof(h), s) != cudaSuccess) return SPEC_ERR_CUDA;
+  *out_status = (h & sv::kStatusTimeout) ? SPEC_ERR_DEVICE_TIMEOUT
+                : (h & sv::kStatusTokenRange) ? SPEC_ERR_TOKEN_RANGE
+                                              : SPEC_OK;
+  return SPEC_OK;
+}
+
+spec_status_t spec_verify_chain(const void* target_logits, const void* draft_logits, int dtype,
+                                const int32_t* tokens, const float* uniforms, int B, int K, int V,
+                                float temperature, const int32_t* depth, int32_t* out_tokens,
+                                int32_t* out_accepted, float* out_alpha, void* workspace,
+                                size_t ws_bytes, void* stream) {
+  VerifyArgs a = {target_logits, draft_logits, dtype, tokens, uniforms, B, K, V, temperature,
+                  depth, -1, out_tokens, out_accepted, out_alpha, nullptr, nullptr, nullptr,
+                  workspace, ws_bytes, static_cast<cudaStream_t>(stream)};
+  return run_verify(a);
+}
+
+spec_status_t spec_verify_block(const void* target_logits, const void* draft_logits, int dtype,
+                                const int32_t* tokens, const float* uniforms, int B, int K, int V,
+                                float temperature, const int32_t* depth, int budget_N,
+                                int32_t* out_tokens, int32_t* out_accepted, float* out_alpha,
+                                float* out_cum_alpha, float* out_expected_len, int32_t* out_depth,
+                                void* workspace, size_t ws_bytes, void* stream) {
+  VerifyArgs a = {target_logits, draft_logits, dtype, tokens, uniforms, B, K, V, temperature,
+                  depth, budget_N, out_tokens, out_accepted, out_alpha, out_cum_alpha,
+                  out_expected_len, out_depth, workspace, ws_bytes, static_cast<cudaStream_t>(stream)};
+  return run_verify(a);
+}
+
+spec_status_t spec_overlap_alpha(const void* target_logits, const void* draft_logits, int dtype,
+                                 int B, int K, int V, float temperature, float* out_alpha,
+                                 float* out_cum_alpha, float* out_expected_len, void* workspace,
+                                 size_t ws_bytes, void* stream) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+  if (B < 0 || K < 0 || V < 1 || bad_T(temperature)) return SPEC_ERR_INVALID_ARG;
+  if (K > sv::kMaxK || V > kMaxV) return SPEC_ERR_UNSUPPORTED;
+  if (B == 0 || K == 0) return SPEC_OK;
+  if (!target_logits || !draft_logits || !out_alpha) return SPEC_ERR_INVALID_ARG;
+  spec_status_t st = check_ws(workspace, ws_bytes, B, K);
+  if (st != SPEC_OK) return st;
+  RowPlan plan;
+  st = plan_rows(target_logits, draft_logits, dtype, B, K, V, temperature, true, true, &plan);
+  if (st != SPEC_OK) return st;
+  const WsLayout L = ws_layout(B, K);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  RowParams& p = plan.p;
+  p.recs = reinterpret_cast<UnitRec*>(ws + L.recs);
+  p.status = reinterpret_cast<int32_t*>(ws + L.status);
+  st = launch_plan(&plan, static_cast<cudaStream_t>(stream));
+  if (st != SPEC_OK) return st;
+  BudgetParams bp;
+  std::memset(&bp, 0, sizeof(bp));
+  bp.recs = p.recs;
+  bp.U = p.U;
+  bp.B = B;
+  bp.K = K;
+  bp.V = V;
+  bp.greedy = temperature == 0.f;
+  bp.stats_only = 1;
+  bp.out_alpha = out_alpha;
+  bp.out_cum = out_cum_alpha;
+  bp.out_E = out_expected_len;
+  bp.status = p.status;
+  return sv::launch_cut(bp, nullptr, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status_t spec_alloc_budget(const float* alpha, int B, int K, int budget_N, int32_t* out_depth,
+                                float* out_conf, void* workspace, size_t ws_bytes, void* stream) {
+  if (B < 0 || K < 0 || budget_N < 0) return SPEC_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * K > kBudgetMaxKeys) return SPEC_ERR_UNSUPPORTED;
+  if (B == 0) return SPEC_OK;
+  if (!out_depth || (K > 0 && !alpha)) return SPEC_ERR_INVALID_ARG;
+  spec_status_t st = check_ws(workspace, ws_bytes, B, K);
+  if (st != SPEC_OK) return st;
+  BudgetParams bp;
+  std::memset(&bp, 0, sizeof(bp));
+  bp.alpha_in = alpha;
+  bp.B = B;
+  bp.K = K;
+  bp.N = budget_N;
+  bp.do_cut = 0;
+  bp.out_depth = out_depth;
+  bp.out_conf = out_conf;
+  bp.status = static_cast<int32_t*>(workspace);
+  return sv::launch_budget_cut(bp, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SPEC_OK
+                                                                                      : SPEC_ERR_CUDA;
+}
+
+void spec_debug_set_wait_limit(long long polls) {
+  g_wait_limit.store(polls < 0 ? kDefaultWaitLimit : polls);
+}
+
+void spec_debug_set_plan(int threads, int cluster, int nstage) {
+  g_force_nt.store(threads == 256 || threads == 512 ? threads : 0);
+  g_force_cluster.store(cluster > 0 && cluster <= sv::kMaxCluster ? cluster : 0);
+  g_force_nstage.store(nstage > 0 && nstage <= 4 ? nstage : 0);
+}
+
+void spec_debug_last_plan(int32_t* out8) {
+  if (out8) std::memcpy(out8, g_last_plan, sizeof(g_last_plan));
+}
+
+}  // extern "C"

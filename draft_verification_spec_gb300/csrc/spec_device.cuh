@@ -1,0 +1,248 @@
+// Device helpers: PTX wrappers for clusters, DSMEM, mbarriers and bulk copies (sm_90+ forms,
+// compiled for sm_103a), warp reductions, and the per-request cut shared by both kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "spec_internal.h"
+
+namespace sv {
+
+__device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
+
+// 2^x with the hardware approximation (MUFU.EX2); flushes denormal results to 0.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- cluster
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_ncta() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_idx() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Full cluster barrier: writes to peers' shared memory before it are visible after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_peer_v4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ void st_peer_v4u(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                            uint32_t d) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
+               "r"(c), "r"(d)
+               : "memory");
+}
+
+// ---------------------------------------------------------------- mbarrier + bulk copy
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase with this parity; false if `limit` polls ran out (limit 0: at once).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit) {
+  if (limit <= 0) return false;
+  for (long long i = 0; i < limit; ++i)
+    if (mbar_try(bar, parity)) return true;
+  return false;
+}
+// Global -> shared bulk copy (16-byte aligned addresses, size a multiple of 16),
+// completion counted on the mbarrier; the L2 is told the source is read once.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// ---------------------------------------------------------------- warp helpers
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+// Butterfly sum: every lane ends with the same value (fp add is commutative).
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ int warp_sum_int(int v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_incl_scan(float v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    float t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    uint64_t t = __shfl_xor_sync(0xffffffffu, v, o);
+    v = t > v ? t : v;
+  }
+  return v;
+}
+
+// Merge two (max, sum of 2^((x - max) c)) pairs; symmetric in its arguments.
+__device__ __forceinline__ void ms_merge(float& m, float& s, float m2, float s2, float c) {
+  const float mn = fmaxf(m, m2);
+  const float ref = (mn == ninf()) ? 0.f : mn;
+  s = s * ex2((m - ref) * c) + s2 * ex2((m2 - ref) * c);
+  m = mn;
+}
+
+// Order-preserving map of a float to uint32 (-0 folded into +0).
+__device__ __forceinline__ uint32_t ord_key(float f) {
+  const uint32_t u = __float_as_uint(f + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+// Argmax key: larger value wins, then the smaller index; 0 means "no element".
+__device__ __forceinline__ uint64_t argmax_key(float v, int idx) {
+  return (static_cast<uint64_t>(ord_key(v)) << 32) | static_cast<uint32_t>(0x7fffffff - idx);
+}
+__device__ __forceinline__ int key_index(uint64_t key) {
+  return 0x7fffffff - static_cast<int>(static_cast<uint32_t>(key & 0xffffffffu));
+}
+
+// First lane (among `valid` lanes) whose running prefix cum0 + incl crosses t; if rounding
+// leaves none, the last valid lane with positive mass; -1 if no lane has mass.  Uniform.
+__device__ __forceinline__ int select_lane(float mass, float cum0, float t, bool valid, int lane,
+                                           float* cum_before) {
+  const float m = valid ? mass : 0.f;
+  const float incl = warp_incl_scan(m, lane);
+  float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 0) excl = 0.f;
+  const unsigned hit = __ballot_sync(0xffffffffu, valid && (cum0 + incl > t));
+  int sel;
+  if (hit) {
+    sel = __ffs(hit) - 1;
+  } else {
+    const unsigned pos = __ballot_sync(0xffffffffu, valid && m > 0.f);
+    sel = pos ? 31 - __clz(pos) : -1;
+  }
+  const float eb = __shfl_sync(0xffffffffu, excl, sel < 0 ? 0 : sel);
+  *cum_before = cum0 + eb;
+  return sel;
+}
+
+__device__ __forceinline__ float ldcg_f(const float* p) { return __ldcg(p); }
+__device__ __forceinline__ int ldcg_i(const int32_t* p) { return __ldcg(p); }
+
+// Serial-acceptance cut of one request, run by one whole warp (lane k <-> position k).
+// Reads the per-row records written by the row kernel; d = verified depth in [0, K].
+__device__ __forceinline__ void cut_request(int b, int d, bool greedy, bool stats_only,
+                                            const UnitRec* recs, int U, int K, int V,
+                                            const int32_t* tokens, const float* uniforms,
+                                            int32_t* out_tokens, int32_t* out_accepted,
+                                            float* out_alpha, float* out_cum, float* out_E,
+                                            int32_t* status, int lane) {
+  const UnitRec* r = recs + static_cast<size_t>(b) * U;
+  // alpha, prefix confidences (left-to-right fp32 product) and expected length
+  const float a = (lane < K) ? ldcg_f(&r[lane].alpha) : 0.f;
+  if (out_alpha && lane < K) out_alpha[static_cast<size_t>(b) * K + lane] = a;
+  if (out_cum || out_E) {
+    float cprod = 1.f, esum = 0.f, mine = 0.f;
+    for (int m = 0; m < K; ++m) {
+      cprod *= __shfl_sync(0xffffffffu, a, m);
+      esum += cprod;
+      if (lane == m) mine = cprod;
+    }
+    if (out_cum && lane < K) out_cum[static_cast<size_t>(b) * K + lane] = mine;
+    if (out_E && lane == 0) out_E[b] = esum;
+  }
+  if (stats_only) return;
+
+  bool ok = true;
+  int x = -1;
+  if (lane < d) {
+    x = tokens[static_cast<size_t>(b) * K + lane];
+    if (x < 0 || x >= V) {
+      ok = false;
+      atomicOr(status, kStatusTokenRange);
+    } else if (greedy) {
+      ok = (x == ldcg_i(&r[lane].g));
+    } else {
+      const float u = uniforms[static_cast<size_t>(b) * (K + 1) + lane];
+      ok = u * ldcg_f(&r[lane].qx) < ldcg_f(&r[lane].px);
+    }
+  }
+  const unsigned rej = __ballot_sync(0xffffffffu, lane < d && !ok);
+  const int n = rej ? __ffs(rej) - 1 : d;
+  int tok = -1;
+  if (lane == 0) {
+    if (greedy) {
+      tok = ldcg_i(&r[n].g);
+    } else if (n < d) {
+      tok = (ldcg_f(&r[n].R) > 0.f) ? ldcg_i(&r[n].rs) : ldcg_i(&r[n].ps);
+    } else {
+      tok = ldcg_i(&r[n].ps);
+    }
+  }
+  tok = __shfl_sync(0xffffffffu, tok, 0);
+  int32_t* ot = out_tokens + static_cast<size_t>(b) * (K + 1);
+  for (int i = lane; i <= K; i += 32) ot[i] = (i < n) ? x : (i == n ? tok : -1);
+  if (lane == 0) out_accepted[b] = n;
+}
+
+}  // namespace sv

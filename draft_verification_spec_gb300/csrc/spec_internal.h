@@ -1,0 +1,79 @@
+// Internal declarations shared by the kernels and the C-ABI host code.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sv {
+
+constexpr int kChunk = 8;         // logits held per register chunk
+constexpr int kNV = 4;            // chunks per thread per row
+constexpr int kMaxCluster = 16;   // CTAs that share one row (non-portable cluster size)
+constexpr int kMaxK = 32;         // drafted positions per request (one warp lane each in the cut)
+
+// Status bits in the workspace's device status word.
+constexpr int kStatusTimeout = 1;
+constexpr int kStatusTokenRange = 2;
+
+// Per (request, position) results of the row kernel; 32 bytes.
+struct UnitRec {
+  float px, qx;      // p_k(x_k), q_k(x_k)
+  float alpha, R;    // overlap sum min(p,q) and residual mass sum max(0, p-q)
+  int32_t rs, ps;    // residual draw, draw from p (bonus candidate); -1 if none
+  int32_t g, gd;     // argmax of the target row, of the draft row (T == 0)
+};
+
+enum : int {
+  F_NEED_DRAFT = 1,   // draft rows are read for positions k < K
+  F_STATS_ONLY = 2,   // rows k < K only; alpha, no draws
+  F_TMA = 8,          // rows are 16-byte aligned: bulk-copy staging ring
+};
+
+struct RowParams {
+  const void* target;        // [B, K+1, V]
+  const void* draft;         // [B, K, V] or null
+  const int32_t* tokens;     // [B, K]
+  const float* uniforms;     // [B, K+1]
+  const int32_t* depth;      // [B] or null
+  int32_t* out_tokens;       // [B, K+1] or null
+  int32_t* out_accepted;     // [B] or null
+  float* out_alpha;          // [B, K] or null
+  float* out_cum;            // [B, K] or null
+  float* out_E;              // [B] or null
+  UnitRec* recs;             // [B, U]
+  int32_t* status;           // 1 word
+  int B, K, V;
+  int U;                     // rows (units) per request: K+1, or K in stats-only mode
+  int total_units;           // B * U
+  int slice;                 // logits per CTA slice (multiple of kChunk)
+  int nstage;                // staging ring depth (TMA path)
+  int stage_row_bytes;       // bytes per row slot in a stage (multiple of 128)
+  int flags;
+  float c;                   // log2(e) / T  (T > 0)
+  long long wait_limit;      // polls per bounded wait; 0 = give up at once
+};
+
+struct BudgetParams {
+  const float* alpha_in;     // [B, K] caller alpha, or null: read recs[b*U + k].alpha
+  const UnitRec* recs;
+  int U;
+  int B, K, V, N;
+  int greedy, do_cut, stats_only;
+  const int32_t* tokens;
+  const float* uniforms;
+  int32_t* out_depth;        // [B] or null
+  float* out_conf;           // [B, K] or null
+  int32_t* out_tokens;
+  int32_t* out_accepted;
+  float* out_alpha;
+  float* out_cum;
+  float* out_E;
+  int32_t* status;
+};
+
+// Host-side launchers of the small kernels (defined next to them).
+cudaError_t launch_budget_cut(const BudgetParams& p, cudaStream_t stream);
+cudaError_t launch_cut(const BudgetParams& p, const int32_t* depth, cudaStream_t stream);
+
+}  // namespace sv

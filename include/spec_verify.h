@@ -1,0 +1,198 @@
+/*
+ * spec_verify.h - C ABI of the batched draft-verification library (sm_103a).
+ *
+ * The operation is speculative-decoding verification as described on the
+ * AngelSpec / DFly pages (agifrontier tutorial, section "KL to end-to-end
+ * TV loss"; abstract; section on verification as a shared batch-level pool):
+ *
+ *   p_k = softmax(z_T[b,k,:] / T),  q_k = softmax(z_D[b,k,:] / T)
+ *   alpha_k = sum_v min(p_k(v), q_k(v)) = 1 - TV(p_k, q_k)
+ *   c_m = prod_{k<=m} alpha_k,   E = sum_{m<K} c_m (expected accepted drafts)
+ *   serial test at k = 0..d_b-1:  accept x_k iff u[b,k] * q_k(x_k) < p_k(x_k);
+ *   the first rejection at n emits a draw from norm(max(0, p_n - q_n)),
+ *   full acceptance emits a bonus draw from p_{d_b};
+ *   T == 0: accept iff x_k == argmax z_T[b,k] (lowest index on ties); the
+ *   emitted token is the target argmax at the first mismatch or at d_b.
+ * Draws use the inverse CDF in vocabulary order: the smallest v whose
+ * inclusive prefix mass is strictly above u[b,K] * (total mass).
+ * The budget spends N verified positions on the N best prefix confidences
+ * c[b,m] over the whole batch (order: c desc, m asc, b asc), which is
+ * prefix-closed and yields a per-request depth d_b.
+ *
+ * Conventions for every entry point
+ * - Pointers named *_logits, tokens, uniforms, depth, out_* and workspace
+ *   are DEVICE pointers (cudaMalloc / torch CUDA memory) on the current
+ *   device; tensors are dense row-major: target [B, K+1, V], draft [B, K, V],
+ *   tokens [B, K] int32, uniforms [B, K+1] float32, outputs as stated.
+ * - The caller owns every buffer.  The library allocates no device memory,
+ *   keeps no per-call state, and never synchronises the stream except in
+ *   spec_get_status.  Every call is asynchronous on `stream` (a cudaStream_t
+ *   passed as void*, NULL = legacy default stream).
+ * - Argument errors are returned synchronously (nothing is launched).
+ *   Data errors found on the device (a draft token outside [0, V), a wait
+ *   that ran out) are recorded in a status word inside the workspace and
+ *   read with spec_get_status.
+ * - The workspace (size from spec_workspace_bytes) holds the status word and
+ *   per-row intermediate records.  Zero-fill it once before its first use
+ *   (spec_workspace_init).  Calls that share a workspace must be ordered on
+ *   one stream.
+ * - A call launches two kernels on `stream`: the row kernel and a small
+ *   kernel (the serial cut, or the budget and the cut) chained to it with
+ *   programmatic dependent launch.
+ * - Logits may contain -inf (probability 0); each row needs one finite
+ *   value.  NaN / +inf give unspecified tokens (they are not scanned for).
+ * - Limits: 1 <= V <= 262144, 0 <= K <= 32, B >= 0 (B == 0 is a no-op),
+ *   T >= 0 and finite.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_ERR_INVALID_ARG = 1,     /* bad pointer, size, dtype, temperature */
+  SPEC_ERR_UNSUPPORTED = 2,     /* shape outside the limits above */
+  SPEC_ERR_CUDA = 3,            /* a launch or runtime call failed */
+  SPEC_ERR_DEVICE_TIMEOUT = 4,  /* a bounded on-device wait ran out */
+  SPEC_ERR_TOKEN_RANGE = 5,     /* a draft token id outside [0, V) */
+  SPEC_ERR_WORKSPACE = 6        /* workspace too small or misaligned */
+} spec_status_t;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int spec_version(void);
+
+/* Static text for a status code. */
+const char* spec_error_string(int status);
+
+/* Bytes of workspace a call with these sizes needs (256-byte aligned start). */
+size_t spec_workspace_bytes(int B, int K, int V, int dtype);
+
+/* Zero-fill a workspace once before its first use (cudaMemsetAsync). */
+spec_status_t spec_workspace_init(void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Read and clear the device status word of a workspace.  Synchronises
+ * `stream`.  *out_status receives SPEC_OK, SPEC_ERR_TOKEN_RANGE or
+ * SPEC_ERR_DEVICE_TIMEOUT (the first two bits found, in that priority:
+ * timeout first).  After SPEC_ERR_DEVICE_TIMEOUT re-initialise the
+ * workspace before reuse.
+ */
+spec_status_t spec_get_status(void* workspace, void* stream, int32_t* out_status);
+
+/*
+ * Verify an MTP chain (K = drafting depth).  Serial acceptance, first
+ * rejection cut, residual / bonus draw (AngelSpec pages, "KL to end-to-end
+ * TV loss": alpha = 1 - TV and the multiplicative, serial acceptance).
+ *
+ *   target_logits [B, K+1, V] dtype; row K is the bonus position.
+ *   draft_logits  [B, K, V] dtype; may be NULL iff temperature == 0 and
+ *                 out_alpha == NULL.
+ *   tokens        [B, K] int32 drafted ids.
+ *   uniforms      [B, K+1] float32 in [0, 1); u[b,k] tests position k,
+ *                 u[b,K] drives the final draw.  Ignored at T == 0 (may be
+ *                 NULL then).
+ *   temperature   T > 0 stochastic, T == 0 greedy; negative or NaN ->
+ *                 SPEC_ERR_INVALID_ARG.
+ *   depth         [B] int32 in [0, K] (e.g. from spec_alloc_budget) or NULL
+ *                 (= K): positions >= depth[b] are not tested and the bonus
+ *                 is drawn at depth[b].  Values outside [0, K] are clamped.
+ *   out_tokens    [B, K+1] int32: accepted drafts, then the emitted token,
+ *                 then -1.
+ *   out_accepted  [B] int32: number n_b of accepted drafts (emitted = n+1).
+ *   out_alpha     [B, K] float32 or NULL (at T == 0: 1 if the argmaxes of
+ *                 target and draft agree, else 0).
+ */
+spec_status_t spec_verify_chain(const void* target_logits, const void* draft_logits, int dtype,
+                                const int32_t* tokens, const float* uniforms,
+                                int B, int K, int V, float temperature,
+                                const int32_t* depth,
+                                int32_t* out_tokens, int32_t* out_accepted, float* out_alpha,
+                                void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Verify a DFly block (K = block size) with the same rule as the chain
+ * (block drafts are accepted left to right, AngelSpec pages, DFly section),
+ * plus the block statistics and, optionally, the batch-level budget:
+ *
+ *   out_cum_alpha    [B, K] float32 prod_{k<=m} alpha_k, or NULL.
+ *   out_expected_len [B] float32 sum_m prod_{k<=m} alpha_k, or NULL
+ *                    (the L_e2e summand of the "KL to end-to-end TV loss"
+ *                    section).
+ *   budget_N         < 0: no budget (depth as in spec_verify_chain);
+ *                    >= 0: spend N verified positions over the batch on the
+ *                    best prefix confidences (the D-cut shared pool, section
+ *                    on verification as a shared batch-level resource); the
+ *                    depth argument must then be NULL.  The logits are read
+ *                    once: alpha of every position, the budget and the
+ *                    decisions come from that one pass.
+ *   out_depth        [B] int32 chosen depth d_b, or NULL.
+ * B * K <= 8192 when budget_N >= 0.  draft_logits is required when
+ * budget_N >= 0 (alpha needs it, also at T == 0).
+ */
+spec_status_t spec_verify_block(const void* target_logits, const void* draft_logits, int dtype,
+                                const int32_t* tokens, const float* uniforms,
+                                int B, int K, int V, float temperature,
+                                const int32_t* depth, int budget_N,
+                                int32_t* out_tokens, int32_t* out_accepted, float* out_alpha,
+                                float* out_cum_alpha, float* out_expected_len, int32_t* out_depth,
+                                void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Overlap statistics only (no decisions): alpha_k for k < K, the prefix
+ * confidences and the expected accepted length (AngelSpec pages, "KL to
+ * end-to-end TV loss", inline formula and L_e2e summand).  Reads target
+ * rows 0..K-1 of the [B, K+1, V] tensor and the [B, K, V] draft tensor.
+ * out_alpha [B, K] required; out_cum_alpha [B, K] and out_expected_len [B]
+ * may be NULL.  T == 0 gives the one-hot limit.
+ */
+spec_status_t spec_overlap_alpha(const void* target_logits, const void* draft_logits, int dtype,
+                                 int B, int K, int V, float temperature,
+                                 float* out_alpha, float* out_cum_alpha, float* out_expected_len,
+                                 void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Batch-level verification budget (AngelSpec abstract and the section on
+ * verification as a shared batch-level resource): alpha [B, K] (device,
+ * float32; clamped to [0, 1], NaN read as 0) -> prefix confidences
+ * c[b,m] = prod_{k<=m} alpha[b,k]; the first min(N, B*K) keys in the order
+ * (c desc, m asc, b asc) are selected; out_depth[b] = number selected in
+ * row b (prefix-closed).  out_conf [B, K] may be NULL.  N >= 0.
+ * B * K <= 8192.  Needs no workspace contents beyond its status word.
+ */
+spec_status_t spec_alloc_budget(const float* alpha, int B, int K, int budget_N,
+                                int32_t* out_depth, float* out_conf,
+                                void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Test hook: iteration limit of every bounded on-device wait (default
+ * 1 << 22 polls).  0 makes every such wait give up at once, which sets
+ * SPEC_ERR_DEVICE_TIMEOUT; in-flight copies are still drained with the
+ * default limit before a kernel returns.  Negative restores the default.
+ * Process-wide; not for production use.
+ */
+void spec_debug_set_wait_limit(long long polls);
+
+/*
+ * Tuning hooks (process-wide, not for production use).  spec_debug_set_plan
+ * forces the row kernel's threads per CTA (256 or 512), cluster size (CTAs
+ * per row, 1..16; must cover V with 32 logits per thread) and staging depth
+ * (1..4); 0 keeps the automatic choice.  spec_debug_last_plan writes the last
+ * launched plan: {threads, cluster, clusters launched, max co-resident
+ * clusters, slice, stages, ring bytes, flags}.
+ */
+void spec_debug_set_plan(int threads, int cluster, int nstage);
+void spec_debug_last_plan(int32_t* out8);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */
