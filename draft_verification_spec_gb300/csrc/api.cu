@@ -11,8 +11,8 @@
 #include "spec_internal.h"
 
 namespace sv {
-const void* row_kernel_bf16(bool greedy, int nt);
-const void* row_kernel_f32(bool greedy, int nt);
+const void* sample_kernel_bf16(int nt);
+const void* sample_kernel_f32(int nt);
 }  // namespace sv
 
 namespace {
@@ -32,15 +32,18 @@ constexpr size_t kRingBudgetLarge = 200 * 1024;   // per CTA when one CTA fills 
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace: [status word | pad to 256] [per-row records, B * (K+1) * 32 bytes]
+// Workspace: [status word | pad to 256] [per-row records, B*(K+1)*32 bytes]
+//            [greedy argmax keys, B*(K+1)*16 bytes; zero between calls]
 struct WsLayout {
-  size_t status, recs, total;
+  size_t status, recs, keys, total;
 };
 WsLayout ws_layout(int B, int K) {
   WsLayout L;
+  const size_t rows = static_cast<size_t>(B > 0 ? B : 1) * (K + 1);
   L.status = 0;
   L.recs = kAlign;
-  L.total = L.recs + align_up(static_cast<size_t>(B > 0 ? B : 1) * (K + 1) * sizeof(UnitRec), kAlign);
+  L.keys = L.recs + align_up(rows * sizeof(UnitRec), kAlign);
+  L.total = L.keys + align_up(rows * 2 * sizeof(uint64_t), kAlign);
   return L;
 }
 
@@ -133,7 +136,8 @@ spec_status_t plan_rows(const void* target, const void* draft, int dtype, int B,
     if (nstage < 1) nstage = 1;
     if (g_force_nstage.load() > 0 && g_force_nstage.load() <= 4) nstage = g_force_nstage.load();
   }
-  plan->fn = bf16 ? sv::row_kernel_bf16(greedy, nt) : sv::row_kernel_f32(greedy, nt);
+  (void)greedy;
+  plan->fn = bf16 ? sv::sample_kernel_bf16(nt) : sv::sample_kernel_f32(nt);
   plan->nt = nt;
   plan->cluster = cluster;
   plan->smem = tma ? static_cast<size_t>(nstage) * stage_bytes : 0;
@@ -187,6 +191,49 @@ spec_status_t launch_plan(RowPlan* plan, cudaStream_t stream) {
 
 bool bad_T(float T) { return !(T >= 0.f) || std::isinf(T); }
 
+// Greedy path: the streaming argmax kernel over target rows (and draft rows when need_draft).
+std::map<int, int> g_argmax_grid;
+spec_status_t launch_greedy(const void* target, const void* draft, int dtype, int B, int K, int V,
+                            bool need_draft, bool stats_only, uint64_t* keys, cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
+  int grid_cap;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_argmax_grid.find(dev * 2 + (dtype == SPEC_BF16));
+    if (it == g_argmax_grid.end()) {
+      int sms = 0, per_sm = 0;
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SPEC_ERR_CUDA;
+      // one wave of resident CTAs (the bf16 and fp32 instances differ only in registers)
+      if (sv::argmax_blocks_per_sm(dtype == SPEC_BF16, &per_sm) != cudaSuccess) return SPEC_ERR_CUDA;
+      g_argmax_grid[dev * 2 + (dtype == SPEC_BF16)] = sms * (per_sm > 0 ? per_sm : 1);
+      it = g_argmax_grid.find(dev * 2 + (dtype == SPEC_BF16));
+    }
+    grid_cap = it->second;
+  }
+  sv::ArgmaxParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.target = target;
+  p.draft = need_draft ? draft : nullptr;
+  p.keys = keys;
+  p.B = B;
+  p.K = K;
+  p.V = V;
+  p.rows_t = stats_only ? K : K + 1;
+  p.tpr = (V + sv::kTileLogits - 1) / sv::kTileLogits;
+  p.total_tiles = (static_cast<long long>(B) * p.rows_t + (need_draft ? static_cast<long long>(B) * K : 0)) * p.tpr;
+  const int esz = dtype == SPEC_BF16 ? 2 : 4;
+  p.aligned = (static_cast<size_t>(V) * esz) % 16 == 0 && aligned16(target) && (!need_draft || aligned16(draft));
+  const long long warps_needed = p.total_tiles;
+  long long grid = (warps_needed + 7) / 8;
+  if (grid > grid_cap) grid = grid_cap;
+  if (grid < 1) grid = 1;
+  if (sv::launch_argmax(dtype == SPEC_BF16, p, static_cast<int>(grid), stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  const int rec[8] = {256, 1, static_cast<int>(grid), grid_cap, sv::kTileLogits, 0, 0, -1};
+  std::memcpy(g_last_plan, rec, sizeof(rec));
+  return SPEC_OK;
+}
+
 spec_status_t check_ws(void* ws, size_t ws_bytes, int B, int K) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return SPEC_ERR_WORKSPACE;
   if (ws_bytes < ws_layout(B, K).total) return SPEC_ERR_WORKSPACE;
@@ -232,30 +279,34 @@ spec_status_t run_verify(const VerifyArgs& a) {
   spec_status_t st = check_ws(a.ws, a.ws_bytes, a.B, a.K);
   if (st != SPEC_OK) return st;
 
-  RowPlan plan;
-  st = plan_rows(a.target, a.draft, a.dtype, a.B, a.K, a.V, a.T, need_draft, false, &plan);
-  if (st != SPEC_OK) return st;
   const WsLayout L = ws_layout(a.B, a.K);
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
-  RowParams& p = plan.p;
-  p.tokens = a.tokens;
-  p.uniforms = a.uniforms;
-  p.depth = a.depth;
-  p.out_tokens = a.out_tokens;
-  p.out_accepted = a.out_accepted;
-  p.out_alpha = a.out_alpha;
-  p.out_cum = a.out_cum;
-  p.out_E = a.out_E;
-  p.recs = reinterpret_cast<UnitRec*>(ws + L.recs);
-  p.status = reinterpret_cast<int32_t*>(ws + L.status);
-  st = launch_plan(&plan, a.stream);
-  if (st != SPEC_OK) return st;
+  UnitRec* recs = reinterpret_cast<UnitRec*>(ws + L.recs);
+  uint64_t* keys = reinterpret_cast<uint64_t*>(ws + L.keys);
+  int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
+  if (greedy) {
+    st = launch_greedy(a.target, a.draft, a.dtype, a.B, a.K, a.V, need_draft, false, keys, a.stream);
+    if (st != SPEC_OK) return st;
+  } else {
+    RowPlan plan;
+    st = plan_rows(a.target, a.draft, a.dtype, a.B, a.K, a.V, a.T, need_draft, false, &plan);
+    if (st != SPEC_OK) return st;
+    RowParams& p = plan.p;
+    p.tokens = a.tokens;
+    p.uniforms = a.uniforms;
+    p.recs = recs;
+    p.status = status;
+    st = launch_plan(&plan, a.stream);
+    if (st != SPEC_OK) return st;
+  }
 
   BudgetParams bp;
   std::memset(&bp, 0, sizeof(bp));
   bp.alpha_in = nullptr;
-  bp.recs = p.recs;
-  bp.U = p.U;
+  bp.recs = recs;
+  bp.keys = keys;
+  bp.draft_keys = greedy && need_draft;
+  bp.U = a.K + 1;
   bp.B = a.B;
   bp.K = a.K;
   bp.V = a.V;
@@ -271,7 +322,7 @@ spec_status_t run_verify(const VerifyArgs& a) {
   bp.out_alpha = a.out_alpha;
   bp.out_cum = a.out_cum;
   bp.out_E = a.out_E;
-  bp.status = p.status;
+  bp.status = status;
   const cudaError_t e = budget ? sv::launch_budget_cut(bp, a.stream) : sv::launch_cut(bp, a.depth, a.stream);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
@@ -356,29 +407,39 @@ spec_status_t spec_overlap_alpha(const void* target_logits, const void* draft_lo
   if (!target_logits || !draft_logits || !out_alpha) return SPEC_ERR_INVALID_ARG;
   spec_status_t st = check_ws(workspace, ws_bytes, B, K);
   if (st != SPEC_OK) return st;
-  RowPlan plan;
-  st = plan_rows(target_logits, draft_logits, dtype, B, K, V, temperature, true, true, &plan);
-  if (st != SPEC_OK) return st;
   const WsLayout L = ws_layout(B, K);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  RowParams& p = plan.p;
-  p.recs = reinterpret_cast<UnitRec*>(ws + L.recs);
-  p.status = reinterpret_cast<int32_t*>(ws + L.status);
-  st = launch_plan(&plan, static_cast<cudaStream_t>(stream));
+  UnitRec* recs = reinterpret_cast<UnitRec*>(ws + L.recs);
+  uint64_t* keys = reinterpret_cast<uint64_t*>(ws + L.keys);
+  int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
+  const bool greedy = temperature == 0.f;
+  if (greedy) {
+    st = launch_greedy(target_logits, draft_logits, dtype, B, K, V, true, true, keys,
+                       static_cast<cudaStream_t>(stream));
+  } else {
+    RowPlan plan;
+    st = plan_rows(target_logits, draft_logits, dtype, B, K, V, temperature, true, true, &plan);
+    if (st != SPEC_OK) return st;
+    plan.p.recs = recs;
+    plan.p.status = status;
+    st = launch_plan(&plan, static_cast<cudaStream_t>(stream));
+  }
   if (st != SPEC_OK) return st;
   BudgetParams bp;
   std::memset(&bp, 0, sizeof(bp));
-  bp.recs = p.recs;
-  bp.U = p.U;
+  bp.recs = recs;
+  bp.keys = keys;
+  bp.draft_keys = greedy;
+  bp.U = K;
   bp.B = B;
   bp.K = K;
   bp.V = V;
-  bp.greedy = temperature == 0.f;
+  bp.greedy = greedy;
   bp.stats_only = 1;
   bp.out_alpha = out_alpha;
   bp.out_cum = out_cum_alpha;
   bp.out_E = out_expected_len;
-  bp.status = p.status;
+  bp.status = status;
   return sv::launch_cut(bp, nullptr, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

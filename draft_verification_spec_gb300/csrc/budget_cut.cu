@@ -1,75 +1,95 @@
-// Batch-level budget (global top-N of prefix confidences, prefix-closed) and the serial cut
-// with the chosen depths.  One warp per request; every CTA rebuilds the confidence table.
+// The small kernels chained after the row kernel:
+//  * cut_kernel: the serial first-rejection cut of each request (one warp per request);
+//  * budget_cut_kernel: the batch-level budget -- the global top-N of prefix confidences
+//    prod_{k<=m} alpha_k, prefix-closed per request -- then the cut at the chosen depths.
+// Both start with griddepcontrol.wait, so they may be scheduled while the row kernel drains.
+#include "argmax_kernel.cuh"
 #include "spec_device.cuh"
 
 namespace sv {
 
 constexpr int kBudgetThreads = 1024;
+constexpr int kCutThreads = 128;
 
 // key (c2, m2, b2) precedes key (c, m, b): c descending, then m ascending, then b ascending
 __device__ __forceinline__ bool precedes(float c2, int m2, int b2, float c, int m, int b) {
   return c2 > c || (c2 == c && (m2 < m || (m2 == m && b2 < b)));
 }
 
+__device__ __forceinline__ float alpha_of(const BudgetParams& P, int b, int k) {
+  if (P.alpha_in) return P.alpha_in[static_cast<size_t>(b) * P.K + k];
+  if (P.greedy) {
+    const unsigned long long* kb = reinterpret_cast<const unsigned long long*>(P.keys) +
+                                   (static_cast<size_t>(b) * (P.K + 1) + k) * 2;
+    return key_index(__ldcg(kb)) == key_index(__ldcg(kb + 1)) ? 1.f : 0.f;
+  }
+  return __ldcg(&P.recs[static_cast<size_t>(b) * P.U + k].alpha);
+}
+
+// One CTA builds the whole confidence table; its warps take requests b = warp, warp + nwarps, ...
+// (grid > 1 only when every CTA can rebuild the table from inputs nobody clears).
 __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid_constant__ BudgetParams P) {
   extern __shared__ float conf[];   // [B, K] prefix confidences
-  asm volatile("griddepcontrol.wait;" ::: "memory");   // the row kernel's records are complete
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // the row kernel's results are complete
   const int B = P.B, K = P.K;
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
     float cp = 1.f;
     for (int k = 0; k < K; ++k) {
-      const float a = P.alpha_in ? P.alpha_in[static_cast<size_t>(b) * K + k]
-                                 : __ldcg(&P.recs[static_cast<size_t>(b) * P.U + k].alpha);
-      cp *= fminf(fmaxf(a, 0.f), 1.f);          // NaN -> 0
+      cp *= fminf(fmaxf(alpha_of(P, b, k), 0.f), 1.f);   // clamp; NaN -> 0
       conf[b * K + k] = cp;
     }
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.x * (kBudgetThreads / 32) + warp;
-  if (b >= B) return;
-
-  // rank of key (b, m) in the total order; within each request b' the preceding keys form a
-  // prefix (conf is non-increasing in m'), found by binary search; lanes split the requests.
-  auto rank_of = [&](int m) {
-    const float cv = conf[b * K + m];
-    int cnt = 0;
-    for (int bp = lane; bp < B; bp += 32) {
-      int lo = 0, hi = K;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (precedes(conf[bp * K + mid], mid, bp, cv, m, b)) lo = mid + 1; else hi = mid;
+  const int nw = blockDim.x >> 5;
+  for (int b = blockIdx.x * nw + warp; b < B; b += gridDim.x * nw) {
+    // rank of key (b, m): within each request b' the keys that precede it form a prefix
+    // (conf is non-increasing in m'), found by binary search; lanes split the requests.
+    auto rank_of = [&](int m) {
+      const float cv = conf[b * K + m];
+      int cnt = 0;
+      for (int bp = lane; bp < B; bp += 32) {
+        int lo = 0, hi = K;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (precedes(conf[bp * K + mid], mid, bp, cv, m, b)) lo = mid + 1; else hi = mid;
+        }
+        cnt += lo;
       }
-      cnt += lo;
+      return warp_sum_int(cnt);
+    };
+    // d_b = number of m whose key ranks below N (a prefix of m)
+    int lo = 0, hi = K;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (rank_of(mid) < P.N) lo = mid + 1; else hi = mid;
     }
-    return warp_sum_int(cnt);
-  };
-  // d_b = number of m whose key ranks below N (a prefix of m)
-  int lo = 0, hi = K;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (rank_of(mid) < P.N) lo = mid + 1; else hi = mid;
+    const int d = lo;
+    if (P.out_depth && lane == 0) P.out_depth[b] = d;
+    if (P.out_conf)
+      for (int k = lane; k < K; k += 32) P.out_conf[static_cast<size_t>(b) * K + k] = conf[b * K + k];
+    if (P.do_cut)
+      cut_request(b, d, P.greedy != 0, P.stats_only != 0, P.recs, P.keys, P.draft_keys != 0, false, P.U, K,
+                  P.V, P.tokens, P.uniforms, P.out_tokens, P.out_accepted, P.out_alpha, P.out_cum, P.out_E,
+                  P.status, lane);
   }
-  const int d = lo;
-  if (P.out_depth && lane == 0) P.out_depth[b] = d;
-  if (P.out_conf)
-    for (int k = lane; k < K; k += 32) P.out_conf[static_cast<size_t>(b) * K + k] = conf[b * K + k];
-  if (P.do_cut)
-    cut_request(b, d, P.greedy != 0, P.stats_only != 0, P.recs, P.U, K, P.V, P.tokens, P.uniforms,
-                P.out_tokens, P.out_accepted, P.out_alpha, P.out_cum, P.out_E, P.status, lane);
+  if (P.greedy && P.keys) {   // every warp of the (single) CTA is done with the keys: clear them
+    __syncthreads();
+    unsigned long long* k = reinterpret_cast<unsigned long long*>(P.keys);
+    for (int i = threadIdx.x; i < B * (K + 1) * 2; i += blockDim.x) k[i] = 0ull;
+  }
 }
 
-// Serial cut only (no budget): one warp per request, depth from the caller or K.
-constexpr int kCutThreads = 128;
 __global__ void __launch_bounds__(kCutThreads) cut_kernel(const __grid_constant__ BudgetParams P,
                                                           const int32_t* depth) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");   // the row kernel's records are complete
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // the row kernel's results are complete
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x * (kCutThreads / 32) + warp;
   if (b >= P.B) return;
   const int d = depth ? min(max(depth[b], 0), P.K) : P.K;
-  cut_request(b, d, P.greedy != 0, P.stats_only != 0, P.recs, P.U, P.K, P.V, P.tokens, P.uniforms,
-              P.out_tokens, P.out_accepted, P.out_alpha, P.out_cum, P.out_E, P.status, lane);
+  cut_request(b, d, P.greedy != 0, P.stats_only != 0, P.recs, P.keys, P.draft_keys != 0, true, P.U, P.K,
+              P.V, P.tokens, P.uniforms, P.out_tokens, P.out_accepted, P.out_alpha, P.out_cum, P.out_E,
+              P.status, lane);
 }
 
 // Launch chained to the previous kernel on the stream (programmatic dependent launch): the
@@ -91,7 +111,8 @@ static cudaError_t launch_pdl(const void* fn, int grid, int block, size_t smem, 
 
 cudaError_t launch_budget_cut(const BudgetParams& p, cudaStream_t stream) {
   const int per = kBudgetThreads / 32;
-  const int grid = (p.B + per - 1) / per;
+  // the greedy path clears the keys it reads, so one CTA must own the whole table
+  const int grid = (p.greedy && p.keys) ? 1 : (p.B + per - 1) / per;
   const size_t smem = static_cast<size_t>(p.B) * p.K * sizeof(float);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(budget_cut_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -100,7 +121,8 @@ cudaError_t launch_budget_cut(const BudgetParams& p, cudaStream_t stream) {
   }
   BudgetParams q = p;
   void* args[] = {&q};
-  return launch_pdl(reinterpret_cast<const void*>(&budget_cut_kernel), grid, kBudgetThreads, smem, stream, args);
+  return launch_pdl(reinterpret_cast<const void*>(&budget_cut_kernel), grid > 0 ? grid : 1, kBudgetThreads,
+                    smem, stream, args);
 }
 
 cudaError_t launch_cut(const BudgetParams& p, const int32_t* depth, cudaStream_t stream) {
@@ -110,6 +132,25 @@ cudaError_t launch_cut(const BudgetParams& p, const int32_t* depth, cudaStream_t
   const int32_t* d = depth;
   void* args[] = {&q, &d};
   return launch_pdl(reinterpret_cast<const void*>(&cut_kernel), grid, kCutThreads, 0, stream, args);
+}
+
+cudaError_t argmax_blocks_per_sm(bool bf16, int* out) {
+  const void* fn = bf16 ? reinterpret_cast<const void*>(&argmax_kernel<true>)
+                        : reinterpret_cast<const void*>(&argmax_kernel<false>);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, fn, 256, 0);
+}
+
+cudaError_t launch_argmax(bool bf16, const ArgmaxParams& p, int grid, cudaStream_t stream) {
+  ArgmaxParams q = p;
+  void* args[] = {&q};
+  const void* fn = bf16 ? reinterpret_cast<const void*>(&argmax_kernel<true>)
+                        : reinterpret_cast<const void*>(&argmax_kernel<false>);
+  // the previous call's cut kernel cleared the keys this grid folds into: plain stream order
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 }  // namespace sv

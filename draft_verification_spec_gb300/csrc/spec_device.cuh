@@ -44,6 +44,10 @@ __device__ __forceinline__ uint32_t cluster_count() {
   return r;
 }
 // Full cluster barrier: writes to peers' shared memory before it are visible after it.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\t"
+               "barrier.cluster.wait.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -62,6 +66,21 @@ __device__ __forceinline__ void st_peer_v4u(uint32_t addr, uint32_t a, uint32_t 
                                             uint32_t d) {
   asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
                "r"(c), "r"(d)
+               : "memory");
+}
+
+// Asynchronous stores into a peer CTA's shared memory; completion is counted (in bytes) on the
+// peer's mbarrier, so the receiver needs no fence and no cluster barrier.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d,
+                                            uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+      "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float a, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(addr), "f"(a),
+               "r"(bar)
                : "memory");
 }
 
@@ -86,6 +105,23 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
+}
+// Acquire at cluster scope: data written into this CTA by peers' st.async is visible after it.
+__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity, long long limit) {
+  for (long long i = 0; i < limit; ++i)
+    if (mbar_try_cluster(bar, parity)) return true;
+  return false;
 }
 // Bounded wait for the phase with this parity; false if `limit` polls ran out (limit 0: at once).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit) {
@@ -190,16 +226,26 @@ __device__ __forceinline__ float ldcg_f(const float* p) { return __ldcg(p); }
 __device__ __forceinline__ int ldcg_i(const int32_t* p) { return __ldcg(p); }
 
 // Serial-acceptance cut of one request, run by one whole warp (lane k <-> position k).
-// Reads the per-row records written by the row kernel; d = verified depth in [0, K].
+// Sampling path: reads the per-row records; greedy path: resolves the argmax keys (and clears
+// them for the next call when `clear_keys`).  d = verified depth in [0, K].
 __device__ __forceinline__ void cut_request(int b, int d, bool greedy, bool stats_only,
-                                            const UnitRec* recs, int U, int K, int V,
+                                            const UnitRec* recs, uint64_t* keys, bool draft_keys,
+                                            bool clear_keys, int U, int K, int V,
                                             const int32_t* tokens, const float* uniforms,
                                             int32_t* out_tokens, int32_t* out_accepted,
                                             float* out_alpha, float* out_cum, float* out_E,
                                             int32_t* status, int lane) {
   const UnitRec* r = recs + static_cast<size_t>(b) * U;
+  uint64_t* kb = keys + static_cast<size_t>(b) * (K + 1) * 2;
+  // greedy: argmax of the target row at this lane's position (and of the draft row)
+  int g = -1, gd = -2;
+  if (greedy && lane < U) {
+    g = key_index(__ldcg(reinterpret_cast<const unsigned long long*>(kb) + 2 * lane));
+    if (draft_keys && lane < K) gd = key_index(__ldcg(reinterpret_cast<const unsigned long long*>(kb) + 2 * lane + 1));
+  }
   // alpha, prefix confidences (left-to-right fp32 product) and expected length
-  const float a = (lane < K) ? ldcg_f(&r[lane].alpha) : 0.f;
+  float a = 0.f;
+  if (lane < K) a = greedy ? (draft_keys && g == gd ? 1.f : 0.f) : ldcg_f(&r[lane].alpha);
   if (out_alpha && lane < K) out_alpha[static_cast<size_t>(b) * K + lane] = a;
   if (out_cum || out_E) {
     float cprod = 1.f, esum = 0.f, mine = 0.f;
@@ -211,38 +257,39 @@ __device__ __forceinline__ void cut_request(int b, int d, bool greedy, bool stat
     if (out_cum && lane < K) out_cum[static_cast<size_t>(b) * K + lane] = mine;
     if (out_E && lane == 0) out_E[b] = esum;
   }
-  if (stats_only) return;
-
-  bool ok = true;
-  int x = -1;
-  if (lane < d) {
-    x = tokens[static_cast<size_t>(b) * K + lane];
-    if (x < 0 || x >= V) {
-      ok = false;
-      atomicOr(status, kStatusTokenRange);
-    } else if (greedy) {
-      ok = (x == ldcg_i(&r[lane].g));
-    } else {
-      const float u = uniforms[static_cast<size_t>(b) * (K + 1) + lane];
-      ok = u * ldcg_f(&r[lane].qx) < ldcg_f(&r[lane].px);
+  if (!stats_only) {
+    bool ok = true;
+    int x = -1;
+    if (lane < d) {
+      x = tokens[static_cast<size_t>(b) * K + lane];
+      if (x < 0 || x >= V) {
+        ok = false;
+        atomicOr(status, kStatusTokenRange);
+      } else if (greedy) {
+        ok = (x == g);
+      } else {
+        const float u = uniforms[static_cast<size_t>(b) * (K + 1) + lane];
+        ok = u * ldcg_f(&r[lane].qx) < ldcg_f(&r[lane].px);
+      }
     }
-  }
-  const unsigned rej = __ballot_sync(0xffffffffu, lane < d && !ok);
-  const int n = rej ? __ffs(rej) - 1 : d;
-  int tok = -1;
-  if (lane == 0) {
+    const unsigned rej = __ballot_sync(0xffffffffu, lane < d && !ok);
+    const int n = rej ? __ffs(rej) - 1 : d;
+    int tok = -1;
     if (greedy) {
-      tok = ldcg_i(&r[n].g);
-    } else if (n < d) {
-      tok = (ldcg_f(&r[n].R) > 0.f) ? ldcg_i(&r[n].rs) : ldcg_i(&r[n].ps);
-    } else {
-      tok = ldcg_i(&r[n].ps);
+      tok = __shfl_sync(0xffffffffu, g, n);
+    } else if (lane == 0) {
+      if (n < d) tok = (ldcg_f(&r[n].R) > 0.f) ? ldcg_i(&r[n].rs) : ldcg_i(&r[n].ps);
+      else tok = ldcg_i(&r[n].ps);
     }
+    tok = __shfl_sync(0xffffffffu, tok, 0);
+    int32_t* ot = out_tokens + static_cast<size_t>(b) * (K + 1);
+    for (int i = lane; i <= K; i += 32) ot[i] = (i < n) ? x : (i == n ? tok : -1);
+    if (lane == 0) out_accepted[b] = n;
   }
-  tok = __shfl_sync(0xffffffffu, tok, 0);
-  int32_t* ot = out_tokens + static_cast<size_t>(b) * (K + 1);
-  for (int i = lane; i <= K; i += 32) ot[i] = (i < n) ? x : (i == n ? tok : -1);
-  if (lane == 0) out_accepted[b] = n;
+  if (greedy && clear_keys && lane < U) {
+    kb[2 * lane] = 0ull;
+    kb[2 * lane + 1] = 0ull;
+  }
 }
 
 }  // namespace sv

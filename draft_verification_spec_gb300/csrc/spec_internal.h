@@ -10,18 +10,32 @@ namespace sv {
 constexpr int kChunk = 8;         // logits held per register chunk
 constexpr int kNV = 4;            // chunks per thread per row
 constexpr int kMaxCluster = 16;   // CTAs that share one row (non-portable cluster size)
-constexpr int kMaxK = 32;         // drafted positions per request (one warp lane each in the cut)
+constexpr int kMaxK = 31;         // drafted positions per request (lanes 0..K of one warp in the cut)
+constexpr int kTileLogits = 32 * kNV * kChunk;   // greedy path: logits per warp tile
 
 // Status bits in the workspace's device status word.
 constexpr int kStatusTimeout = 1;
 constexpr int kStatusTokenRange = 2;
 
-// Per (request, position) results of the row kernel; 32 bytes.
+// Per (request, position) results of the sampling row kernel; 32 bytes.
 struct UnitRec {
   float px, qx;      // p_k(x_k), q_k(x_k)
   float alpha, R;    // overlap sum min(p,q) and residual mass sum max(0, p-q)
   int32_t rs, ps;    // residual draw, draw from p (bonus candidate); -1 if none
-  int32_t g, gd;     // argmax of the target row, of the draft row (T == 0)
+  int32_t pad0, pad1;
+};
+// Greedy path: per (request, position) two 64-bit argmax keys (target row, draft row), folded
+// with atomicMax by the argmax kernel and cleared by the kernel that consumes them.
+
+struct ArgmaxParams {
+  const void* target;        // [B, K+1, V]
+  const void* draft;         // [B, K, V] or null
+  uint64_t* keys;            // [B, K+1, 2]
+  int B, K, V;
+  int rows_t;                // target rows scanned per request (K+1, or K for overlap stats)
+  int tpr;                   // tiles per row
+  long long total_tiles;     // (B*rows_t + B*K*need_draft) * tpr
+  int aligned;               // rows start on 16-byte boundaries
 };
 
 enum : int {
@@ -55,8 +69,10 @@ struct RowParams {
 };
 
 struct BudgetParams {
-  const float* alpha_in;     // [B, K] caller alpha, or null: read recs[b*U + k].alpha
+  const float* alpha_in;     // [B, K] caller alpha, or null: from recs / keys
   const UnitRec* recs;
+  uint64_t* keys;            // greedy path: argmax keys [B, K+1, 2] (cleared after use)
+  int draft_keys;            // greedy path: draft keys were produced (one-hot alpha)
   int U;
   int B, K, V, N;
   int greedy, do_cut, stats_only;
@@ -73,6 +89,8 @@ struct BudgetParams {
 };
 
 // Host-side launchers of the small kernels (defined next to them).
+cudaError_t launch_argmax(bool bf16, const ArgmaxParams& p, int grid, cudaStream_t stream);
+cudaError_t argmax_blocks_per_sm(bool bf16, int* out);
 cudaError_t launch_budget_cut(const BudgetParams& p, cudaStream_t stream);
 cudaError_t launch_cut(const BudgetParams& p, const int32_t* depth, cudaStream_t stream);
 

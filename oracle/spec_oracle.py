@@ -131,6 +131,8 @@ class VerifyResult:
 def _first_false(ok: np.ndarray, d: np.ndarray) -> np.ndarray:
     """Index of the first False among positions k < d[b] of ok[b, :], else d[b]."""
     B, K = ok.shape
+    if K == 0:                      # nothing drafted: d is 0 and the chain ends at position 0
+        return d.copy()
     k = np.arange(K)[None, :]
     stop = (~ok) & (k < d[:, None])
     return np.where(np.any(stop, axis=1), np.argmax(stop, axis=1), d)

@@ -240,6 +240,18 @@ def test_alpha_zero_always_rejects_at_zero():
     assert _chi2_ok(toks[:, 0], p0)
 
 
+def test_no_drafts_is_plain_decoding():
+    """K = 0: one token per request, the target argmax at T = 0 and a draw from p_0 at T > 0."""
+    zt = np.random.default_rng(12).normal(0, 1.5, (1, 9))
+    r = O.verify(zt[None], None, np.zeros((1, 0), dtype=int), np.zeros((1, 1)), 0.0)
+    assert r.accepted[0] == 0 and r.tokens[0, 0] == int(np.argmax(zt[0]))
+    n = 200_000
+    u = np.random.default_rng(13).random((n, 1))
+    r = O.verify(np.broadcast_to(zt, (n, 1, 9)), np.zeros((n, 0, 9)), np.zeros((n, 0), dtype=int), u, 0.8)
+    assert np.all(r.accepted == 0)
+    assert _chi2_ok(r.tokens[:, 0], scipy.special.softmax(zt[0] / 0.8))
+
+
 # ---------------------------------------------------------------- greedy
 
 def test_greedy_acceptance_is_argmax_agreement():
