@@ -134,7 +134,7 @@ class VerifyOutput:
     depth: Optional[torch.Tensor] = None
 
 
-def _validate(target, draft, tokens, uniforms, temperature, draft_needed):
+def _validate(target, draft, tokens, uniforms, temperature, draft_needed, tokens_needed=True):
     if target.dim() != 3:
         raise ValueError("target logits must be [B, K+1, V]")
     B, K1, V = target.shape
@@ -146,11 +146,11 @@ def _validate(target, draft, tokens, uniforms, temperature, draft_needed):
         _need(draft, "draft", dtype=target.dtype, shape=(B, K, V), device=dev)
     elif draft_needed:
         raise ValueError("draft logits are required here")
-    if K > 0:
+    if K > 0 and tokens_needed:
         if tokens is None:
             raise ValueError("tokens [B, K] are required")
         _need(tokens, "tokens", dtype=torch.int32, shape=(B, K), device=dev)
-    if temperature > 0:
+    if temperature > 0 and tokens_needed:
         if uniforms is None:
             raise ValueError("uniforms [B, K+1] are required at T > 0")
         _need(uniforms, "uniforms", dtype=torch.float32, shape=(B, K1), device=dev)
@@ -212,7 +212,7 @@ def verify_block(target, draft, tokens, uniforms, temperature: float, depth=None
 
 def overlap_alpha(target, draft, temperature: float, stream=None, workspace: Optional[Workspace] = None):
     """alpha [B, K], prefix confidences [B, K], expected length [B] (spec_overlap_alpha)."""
-    B, K, V, code = _validate(target, draft, None, None, 0.0, draft_needed=True)
+    B, K, V, code = _validate(target, draft, None, None, temperature, draft_needed=True, tokens_needed=False)
     dev = target.device
     alpha = torch.empty(B, K, dtype=torch.float32, device=dev)
     cum = torch.empty(B, K, dtype=torch.float32, device=dev)

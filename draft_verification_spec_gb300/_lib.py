@@ -34,6 +34,7 @@ SIGNATURES = {
     "spec_debug_set_wait_limit": (None, [c_longlong]),
     "spec_debug_set_plan": (None, [c_int, c_int, c_int]),
     "spec_debug_last_plan": (None, [c_void_p]),
+    "spec_debug_set_variant": (None, [c_int]),
 }
 
 _lib = None

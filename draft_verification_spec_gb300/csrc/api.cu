@@ -32,23 +32,34 @@ constexpr size_t kRingBudgetLarge = 200 * 1024;   // per CTA when one CTA fills 
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace: [status word | pad to 256] [per-row records, B*(K+1)*32 bytes]
-//            [greedy argmax keys, B*(K+1)*16 bytes; zero between calls]
+// Workspace layout, a function of the buffer size only (so the greedy keys, which the cut
+// kernel clears after every call, never overlap bytes another call shape wrote):
+//   [status word | pad to 256] [argmax keys: cap rows x 16 B] [request counters: cap x 4 B]
+//   [row records: cap rows x 32 B]
+// where cap = the number of (request, position) rows the buffer can hold.
+constexpr size_t kKeyBytes = 2 * sizeof(uint64_t);
+constexpr size_t kRowBytes = kKeyBytes + sizeof(int32_t) + sizeof(UnitRec);
 struct WsLayout {
-  size_t status, recs, keys, total;
+  size_t status, keys, counters, recs, cap_rows;
 };
-WsLayout ws_layout(int B, int K) {
+WsLayout ws_layout_for(size_t ws_bytes) {
   WsLayout L;
-  const size_t rows = static_cast<size_t>(B > 0 ? B : 1) * (K + 1);
   L.status = 0;
-  L.recs = kAlign;
-  L.keys = L.recs + align_up(rows * sizeof(UnitRec), kAlign);
-  L.total = L.keys + align_up(rows * 2 * sizeof(uint64_t), kAlign);
+  L.keys = kAlign;
+  const size_t avail = ws_bytes > 4 * kAlign ? ws_bytes - 4 * kAlign : 0;
+  L.cap_rows = avail / kRowBytes;
+  L.counters = align_up(L.keys + L.cap_rows * kKeyBytes, kAlign);
+  L.recs = align_up(L.counters + L.cap_rows * sizeof(int32_t), kAlign);
   return L;
+}
+size_t ws_bytes_needed(int B, int K) {
+  const size_t rows = static_cast<size_t>(B > 0 ? B : 1) * (K + 1);
+  return 4 * kAlign + rows * kRowBytes;
 }
 
 // Test and tuning hooks: the last row-kernel plan, and optional overrides (0 = automatic).
 std::atomic<int> g_force_nt{0}, g_force_cluster{0}, g_force_nstage{0};
+std::atomic<int> g_variant{0};   // greedy path: bit 1 separate cut kernel
 int g_last_plan[8] = {0};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -192,27 +203,34 @@ spec_status_t launch_plan(RowPlan* plan, cudaStream_t stream) {
 bool bad_T(float T) { return !(T >= 0.f) || std::isinf(T); }
 
 // Greedy path: the streaming argmax kernel over target rows (and draft rows when need_draft).
+// Ring: stages of 8 tiles (16 KB bf16 / 32 KB fp32); about 64 KB per CTA.
+int argmax_stages(int dtype) {
+  if (g_force_nstage.load() > 0) return g_force_nstage.load() > 8 ? 8 : g_force_nstage.load();
+  return dtype == SPEC_BF16 ? 4 : 2;
+}
 std::map<int, int> g_argmax_grid;
 spec_status_t launch_greedy(const void* target, const void* draft, int dtype, int B, int K, int V,
-                            bool need_draft, bool stats_only, uint64_t* keys, cudaStream_t stream) {
+                            bool need_draft, bool stats_only, bool fused_cut, uint64_t* keys,
+                            sv::ArgmaxParams cut, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
   int grid_cap;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    auto it = g_argmax_grid.find(dev * 2 + (dtype == SPEC_BF16));
+    const int gkey = dev * 64 + (dtype == SPEC_BF16) * 16 + argmax_stages(dtype);
+    auto it = g_argmax_grid.find(gkey);
     if (it == g_argmax_grid.end()) {
       int sms = 0, per_sm = 0;
       if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SPEC_ERR_CUDA;
       // one wave of resident CTAs (the bf16 and fp32 instances differ only in registers)
-      if (sv::argmax_blocks_per_sm(dtype == SPEC_BF16, &per_sm) != cudaSuccess) return SPEC_ERR_CUDA;
-      g_argmax_grid[dev * 2 + (dtype == SPEC_BF16)] = sms * (per_sm > 0 ? per_sm : 1);
-      it = g_argmax_grid.find(dev * 2 + (dtype == SPEC_BF16));
+      if (sv::argmax_blocks_per_sm(dtype == SPEC_BF16, argmax_stages(dtype), &per_sm) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+      g_argmax_grid[gkey] = sms * (per_sm > 0 ? per_sm : 1);
+      it = g_argmax_grid.find(gkey);
     }
     grid_cap = it->second;
   }
-  sv::ArgmaxParams p;
-  std::memset(&p, 0, sizeof(p));
+  sv::ArgmaxParams p = cut;   // fused-cut arguments (tokens, depth, outputs, counters, status)
   p.target = target;
   p.draft = need_draft ? draft : nullptr;
   p.keys = keys;
@@ -220,8 +238,16 @@ spec_status_t launch_greedy(const void* target, const void* draft, int dtype, in
   p.K = K;
   p.V = V;
   p.rows_t = stats_only ? K : K + 1;
-  p.tpr = (V + sv::kTileLogits - 1) / sv::kTileLogits;
-  p.total_tiles = (static_cast<long long>(B) * p.rows_t + (need_draft ? static_cast<long long>(B) * K : 0)) * p.tpr;
+  p.drows = need_draft ? K : 0;
+  const int tile = dtype == SPEC_BF16 ? 2048 : 1024;   // the argmax kernel's warp tile
+  p.tpr = (V + tile - 1) / tile;
+  p.total_tiles = static_cast<long long>(B) * (p.rows_t + p.drows) * p.tpr;
+  if (p.total_tiles >= (1ll << 31)) return SPEC_ERR_UNSUPPORTED;
+  const int variant = g_variant.load();
+  p.fused_cut = fused_cut && !(variant & 2);
+  p.stats_only = stats_only;
+  p.nstage = argmax_stages(dtype);
+  p.wait_limit = g_wait_limit.load();
   const int esz = dtype == SPEC_BF16 ? 2 : 4;
   p.aligned = (static_cast<size_t>(V) * esz) % 16 == 0 && aligned16(target) && (!need_draft || aligned16(draft));
   const long long warps_needed = p.total_tiles;
@@ -229,14 +255,16 @@ spec_status_t launch_greedy(const void* target, const void* draft, int dtype, in
   if (grid > grid_cap) grid = grid_cap;
   if (grid < 1) grid = 1;
   if (sv::launch_argmax(dtype == SPEC_BF16, p, static_cast<int>(grid), stream) != cudaSuccess) return SPEC_ERR_CUDA;
-  const int rec[8] = {256, 1, static_cast<int>(grid), grid_cap, sv::kTileLogits, 0, 0, -1};
+  const int rec[8] = {256, 1, static_cast<int>(grid), grid_cap, tile, 0,
+                      0, -1};
   std::memcpy(g_last_plan, rec, sizeof(rec));
   return SPEC_OK;
 }
 
 spec_status_t check_ws(void* ws, size_t ws_bytes, int B, int K) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return SPEC_ERR_WORKSPACE;
-  if (ws_bytes < ws_layout(B, K).total) return SPEC_ERR_WORKSPACE;
+  if (ws_bytes < ws_bytes_needed(B, K)) return SPEC_ERR_WORKSPACE;
+  if (ws_layout_for(ws_bytes).cap_rows < static_cast<size_t>(B) * (K + 1)) return SPEC_ERR_WORKSPACE;
   return SPEC_OK;
 }
 
@@ -279,14 +307,28 @@ spec_status_t run_verify(const VerifyArgs& a) {
   spec_status_t st = check_ws(a.ws, a.ws_bytes, a.B, a.K);
   if (st != SPEC_OK) return st;
 
-  const WsLayout L = ws_layout(a.B, a.K);
+  const WsLayout L = ws_layout_for(a.ws_bytes);
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
   UnitRec* recs = reinterpret_cast<UnitRec*>(ws + L.recs);
   uint64_t* keys = reinterpret_cast<uint64_t*>(ws + L.keys);
+  int32_t* counters = reinterpret_cast<int32_t*>(ws + L.counters);
   int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
   if (greedy) {
-    st = launch_greedy(a.target, a.draft, a.dtype, a.B, a.K, a.V, need_draft, false, keys, a.stream);
+    sv::ArgmaxParams cut;
+    std::memset(&cut, 0, sizeof(cut));
+    cut.counters = counters;
+    cut.status = status;
+    cut.tokens = a.tokens;
+    cut.depth = a.depth;
+    cut.out_tokens = a.out_tokens;
+    cut.out_accepted = a.out_accepted;
+    cut.out_alpha = a.out_alpha;
+    cut.out_cum = a.out_cum;
+    cut.out_E = a.out_E;
+    st = launch_greedy(a.target, a.draft, a.dtype, a.B, a.K, a.V, need_draft, false, !budget, keys, cut,
+                       a.stream);
     if (st != SPEC_OK) return st;
+    if (!budget && (g_variant.load() & 2) == 0) return SPEC_OK;   // the cut ran inside the argmax kernel
   } else {
     RowPlan plan;
     st = plan_rows(a.target, a.draft, a.dtype, a.B, a.K, a.V, a.T, need_draft, false, &plan);
@@ -294,8 +336,10 @@ spec_status_t run_verify(const VerifyArgs& a) {
     RowParams& p = plan.p;
     p.tokens = a.tokens;
     p.uniforms = a.uniforms;
+    p.depth = a.depth;
     p.recs = recs;
     p.status = status;
+    if (budget) p.flags |= sv::F_ALL_PDRAWS;
     st = launch_plan(&plan, a.stream);
     if (st != SPEC_OK) return st;
   }
@@ -350,7 +394,7 @@ size_t spec_workspace_bytes(int B, int K, int V, int dtype) {
   (void)V;
   (void)dtype;
   if (B < 0 || K < 0) return 0;
-  return ws_layout(B, K).total;
+  return ws_bytes_needed(B, K);
 }
 
 spec_status_t spec_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
@@ -407,15 +451,23 @@ spec_status_t spec_overlap_alpha(const void* target_logits, const void* draft_lo
   if (!target_logits || !draft_logits || !out_alpha) return SPEC_ERR_INVALID_ARG;
   spec_status_t st = check_ws(workspace, ws_bytes, B, K);
   if (st != SPEC_OK) return st;
-  const WsLayout L = ws_layout(B, K);
+  const WsLayout L = ws_layout_for(ws_bytes);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   UnitRec* recs = reinterpret_cast<UnitRec*>(ws + L.recs);
   uint64_t* keys = reinterpret_cast<uint64_t*>(ws + L.keys);
   int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
   const bool greedy = temperature == 0.f;
   if (greedy) {
-    st = launch_greedy(target_logits, draft_logits, dtype, B, K, V, true, true, keys,
+    sv::ArgmaxParams cut;
+    std::memset(&cut, 0, sizeof(cut));
+    cut.counters = reinterpret_cast<int32_t*>(ws + L.counters);
+    cut.status = status;
+    cut.out_alpha = out_alpha;
+    cut.out_cum = out_cum_alpha;
+    cut.out_E = out_expected_len;
+    st = launch_greedy(target_logits, draft_logits, dtype, B, K, V, true, true, true, keys, cut,
                        static_cast<cudaStream_t>(stream));
+    if (st != SPEC_OK || (g_variant.load() & 2) == 0) return st;
   } else {
     RowPlan plan;
     st = plan_rows(target_logits, draft_logits, dtype, B, K, V, temperature, true, true, &plan);
@@ -474,6 +526,8 @@ void spec_debug_set_plan(int threads, int cluster, int nstage) {
   g_force_cluster.store(cluster > 0 && cluster <= sv::kMaxCluster ? cluster : 0);
   g_force_nstage.store(nstage > 0 && nstage <= 4 ? nstage : 0);
 }
+
+void spec_debug_set_variant(int variant) { g_variant.store(variant & 3); }
 
 void spec_debug_last_plan(int32_t* out8) {
   if (out8) std::memcpy(out8, g_last_plan, sizeof(g_last_plan));

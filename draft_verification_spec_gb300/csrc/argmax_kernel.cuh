@@ -1,40 +1,39 @@
 // Greedy-path row kernel (T == 0): argmax of every target row (and of the draft rows when the
-// one-hot alpha is wanted), lowest index on ties.  No cross-CTA dependency: each warp scans
-// 1024-logit tiles (grid-stride over all rows' tiles) with 16-byte loads prefetched one tile
-// ahead in registers, reduces a 64-bit (value, lowest index) key over the warp and folds it into
-// the row's slot with atomicMax.  The cut kernel resolves and clears the slots.
+// one-hot alpha is wanted), lowest index on ties, fused with the serial cut.
+//
+// The rows are cut into warp tiles (2048 bf16 / 1024 fp32 logits in 16-byte chunks), ordered request by
+// request; each warp takes one contiguous run of tiles and streams it with 16-byte loads (the
+// other resident warps cover their latency).  Per tile: packed bf16 max (HMNMX2) per lane, warp max,
+// then only lanes holding the maximum look for its first index.  Keys (value, lowest index) of
+// one row are folded in registers and published with one atomicMax per row segment; a
+// release-add per request segment counts finished tiles, and the warp that completes a request
+// runs its cut and clears the request's slots and counter for the next call.  No CTA barrier.
 #pragma once
 
 #include <climits>
+#include <cuda_bf16.h>
 
 #include "spec_device.cuh"
 
 namespace sv {
 
-constexpr int kTile = kTileLogits;   // logits per warp tile (1024)
-
-template <bool BF16>
-struct TileRegs {
-  static constexpr int kWords = BF16 ? kNV : 2 * kNV;   // uint4 per lane per tile
-  uint4 w[kWords];
+// Tile geometry: bf16 lanes hold 8 chunks of 8 logits (one 16-byte load each), fp32 lanes 4
+// chunks of 8 logits (two 16-byte loads each); a warp tile is 32 lanes of that.
+template <bool BF16> struct Geo {
+  static constexpr int kChunks = BF16 ? 8 : 4;          // chunks per lane
+  static constexpr int kWords = BF16 ? 8 : 8;           // uint4 per lane
+  static constexpr int kTile = 32 * kChunks * kChunk;   // logits per warp tile (2048 / 1024)
 };
 
 template <bool BF16>
-__device__ __forceinline__ void load_tile(TileRegs<BF16>& r, const uint8_t* row, int base, int V, int lane) {
-  constexpr int ESZ = BF16 ? 2 : 4;
-#pragma unroll
-  for (int j = 0; j < kNV; ++j) {
-    const int e0 = base + (j * 32 + lane) * kChunk;
-    if (e0 + kChunk <= V) {
-      const uint4* p = reinterpret_cast<const uint4*>(row + static_cast<size_t>(e0) * ESZ);
-      if constexpr (BF16) {
-        r.w[j] = __ldcs(p);
-      } else {
-        r.w[2 * j] = __ldcs(p);
-        r.w[2 * j + 1] = __ldcs(p + 1);
-      }
-    }
-  }
+struct TileRegs {
+  uint4 w[Geo<BF16>::kWords];
+};
+
+__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t u) {
+  __nv_bfloat162 r;
+  memcpy(&r, &u, sizeof(r));
+  return r;
 }
 
 template <bool BF16>
@@ -50,94 +49,221 @@ __device__ __forceinline__ float tile_elem(const TileRegs<BF16>& r, int j, int e
   }
 }
 
-// Scan one tile (aligned rows: from prefetched registers; otherwise element-wise loads).
+// Load one tile; chunks past the row end read as -inf (their logits do not exist).
 template <bool BF16>
-__device__ __forceinline__ uint64_t tile_key(const TileRegs<BF16>& r, const uint8_t* row, int base, int V,
-                                             int lane, bool aligned) {
+__device__ __forceinline__ void load_tile(TileRegs<BF16>& r, const uint8_t* row, int base, int V, int lane) {
   constexpr int ESZ = BF16 ? 2 : 4;
-  float best = ninf();
-  int bi = INT_MAX;
+  constexpr uint32_t NEG = BF16 ? 0xff80ff80u : 0xff800000u;
 #pragma unroll
-  for (int j = 0; j < kNV; ++j) {
+  for (int j = 0; j < Geo<BF16>::kChunks; ++j) {
     const int e0 = base + (j * 32 + lane) * kChunk;
-    if (aligned && e0 + kChunk <= V) {
-      if (bi == INT_MAX) bi = e0;            // first logit this lane sees (covers all -inf)
-#pragma unroll
-      for (int e = 0; e < kChunk; ++e) {
-        const float x = tile_elem<BF16>(r, j, e);
-        if (x > best) { best = x; bi = e0 + e; }
+    const uint4* p = reinterpret_cast<const uint4*>(row + static_cast<size_t>(e0) * ESZ);
+    if (e0 + kChunk <= V) {
+      if constexpr (BF16) {
+        r.w[j] = __ldcs(p);
+      } else {
+        r.w[2 * j] = __ldcs(p);
+        r.w[2 * j + 1] = __ldcs(p + 1);
       }
     } else {
+      uint32_t v[kChunk * ESZ / 4];
+#pragma unroll
+      for (int i = 0; i < kChunk * ESZ / 4; ++i) v[i] = NEG;
 #pragma unroll
       for (int e = 0; e < kChunk; ++e) {
         if (e0 + e < V) {
-          float x;
           if constexpr (BF16) {
-            x = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(row)[e0 + e]) << 16);
+            const uint32_t h = reinterpret_cast<const uint16_t*>(row)[e0 + e];
+            v[e >> 1] = (e & 1) ? ((v[e >> 1] & 0x0000ffffu) | (h << 16)) : ((v[e >> 1] & 0xffff0000u) | h);
           } else {
-            x = reinterpret_cast<const float*>(row)[e0 + e];
+            v[e] = reinterpret_cast<const uint32_t*>(row)[e0 + e];
           }
-          if (bi == INT_MAX) bi = e0 + e;
-          if (x > best) { best = x; bi = e0 + e; }
         }
+      }
+      if constexpr (BF16) {
+        r.w[j] = make_uint4(v[0], v[1], v[2], v[3]);
+      } else {
+        r.w[2 * j] = make_uint4(v[0], v[1], v[2], v[3]);
+        r.w[2 * j + 1] = make_uint4(v[4], v[5], v[6], v[7]);
       }
     }
   }
-  (void)ESZ;
-  return bi == INT_MAX ? 0ull : argmax_key(best, bi);
 }
 
+// Warp argmax key of a tile in registers: per-chunk maxima, lane max, warp max; then only lanes
+// holding the maximum find its first chunk and the first logit in it (lowest index wins).
 template <bool BF16>
-__global__ void __launch_bounds__(256) argmax_kernel(const __grid_constant__ ArgmaxParams P) {
-  constexpr int ESZ = BF16 ? 2 : 4;
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int lane = threadIdx.x & 31;
-  const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-  const long long trows = static_cast<long long>(P.B) * P.rows_t;
-  const int K = P.K, V = P.V, tpr = P.tpr;
+__device__ __forceinline__ uint64_t tile_key_regs(const TileRegs<BF16>& r, int base, int lane) {
+  constexpr int NC = Geo<BF16>::kChunks;
+  float cm[NC];
+  if constexpr (BF16) {
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+      const __nv_bfloat162 m = __hmax2(__hmax2(as_bf2(r.w[j].x), as_bf2(r.w[j].y)),
+                                       __hmax2(as_bf2(r.w[j].z), as_bf2(r.w[j].w)));
+      cm[j] = fmaxf(__low2float(m), __high2float(m));
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+      float a = fmaxf(tile_elem<false>(r, j, 0), tile_elem<false>(r, j, 1));
+      float b = fmaxf(tile_elem<false>(r, j, 2), tile_elem<false>(r, j, 3));
+      float c = fmaxf(tile_elem<false>(r, j, 4), tile_elem<false>(r, j, 5));
+      float d = fmaxf(tile_elem<false>(r, j, 6), tile_elem<false>(r, j, 7));
+      cm[j] = fmaxf(fmaxf(a, b), fmaxf(c, d));
+    }
+  }
+  float lm = cm[0];
+#pragma unroll
+  for (int j = 1; j < NC; ++j) lm = fmaxf(lm, cm[j]);
+  const float wm = warp_max(lm);
+  int idx = INT_MAX;
+  if (lm == wm) {   // usually one lane
+    int jf = NC - 1;
+#pragma unroll
+    for (int j = NC - 1; j >= 0; --j)
+      if (cm[j] == wm) jf = j;
+    int ef = kChunk - 1;
+#pragma unroll
+    for (int j = 0; j < NC; ++j)
+      if (j == jf) {
+#pragma unroll
+        for (int e = kChunk - 1; e >= 0; --e)
+          if (tile_elem<BF16>(r, j, e) == wm) ef = e;
+      }
+    idx = base + (jf * 32 + lane) * kChunk + ef;
+  }
+  idx = __reduce_min_sync(0xffffffffu, idx);
+  if (idx == INT_MAX) idx = base;   // NaN maximum: unspecified, keep the index in range
+  return argmax_key(wm, idx);
+}
 
-  auto locate = [&](long long t, const uint8_t*& row, int& base, size_t& slot) {
-    const long long r = t / tpr;
-    base = static_cast<int>(t - r * tpr) * kTile;
-    if (r < trows) {
-      const long long b = r / P.rows_t, k = r - b * P.rows_t;
-      row = static_cast<const uint8_t*>(P.target) + ((b * (K + 1) + k) * static_cast<size_t>(V)) * ESZ;
-      slot = static_cast<size_t>(b * (K + 1) + k) * 2;
+// Partial or unaligned tile: element-wise loads with bounds checks.
+template <bool BF16>
+__device__ __forceinline__ uint64_t tile_key_scalar(const uint8_t* row, int base, int V, int lane) {
+  float best = ninf();
+  int bi = INT_MAX;
+#pragma unroll
+  for (int j = 0; j < Geo<BF16>::kChunks; ++j) {
+    const int e0 = base + (j * 32 + lane) * kChunk;
+#pragma unroll
+    for (int e = 0; e < kChunk; ++e) {
+      if (e0 + e < V) {
+        float x;
+        if constexpr (BF16) {
+          x = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(row)[e0 + e]) << 16);
+        } else {
+          x = reinterpret_cast<const float*>(row)[e0 + e];
+        }
+        if (bi == INT_MAX) bi = e0 + e;     // the first logit this lane sees (covers all -inf)
+        if (x > best) { best = x; bi = e0 + e; }
+      }
+    }
+  }
+  uint64_t key = bi == INT_MAX ? 0ull : argmax_key(best, bi);
+  return warp_max_u64(key);
+}
+
+// Position of a tile in the request-major tile order, advanced without divisions.
+struct TileCursor {
+  const uint8_t* row;
+  int base, q, req, slot;
+};
+
+template <bool BF16>
+__global__ void __launch_bounds__(256, BF16 ? 4 : 2) argmax_kernel(const __grid_constant__ ArgmaxParams P) {
+  constexpr int ESZ = BF16 ? 2 : 4;
+  constexpr int NWARP = 8;
+  constexpr int kTile = Geo<BF16>::kTile;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = P.K, V = P.V, tpr = P.tpr;
+  const int rows_req = P.rows_t + P.drows;            // rows per request: target, then draft
+  const int tiles_req = rows_req * tpr;
+  const int total = static_cast<int>(P.total_tiles);  // < 2^31 (checked by the host)
+  // this warp's contiguous run of tiles
+  const long long gw = static_cast<long long>(blockIdx.x) * NWARP + warp, nw = static_cast<long long>(gridDim.x) * NWARP;
+  const int t0 = static_cast<int>(gw * total / nw), t1 = static_cast<int>((gw + 1) * total / nw);
+  if (t0 >= t1) return;
+
+  auto set_row = [&](TileCursor& c) {
+    if (c.q < P.rows_t) {
+      c.row = static_cast<const uint8_t*>(P.target) + ((static_cast<size_t>(c.req) * (K + 1) + c.q) * V) * ESZ;
+      c.slot = (c.req * (K + 1) + c.q) * 2;
     } else {
-      const long long rr = r - trows, b = rr / K, k = rr - b * K;
-      row = static_cast<const uint8_t*>(P.draft) + ((b * K + k) * static_cast<size_t>(V)) * ESZ;
-      slot = static_cast<size_t>(b * (K + 1) + k) * 2 + 1;
+      const int k = c.q - P.rows_t;
+      c.row = static_cast<const uint8_t*>(P.draft) + ((static_cast<size_t>(c.req) * K + k) * V) * ESZ;
+      c.slot = (c.req * (K + 1) + k) * 2 + 1;
+    }
+  };
+  auto step = [&](TileCursor& c) {
+    c.base += kTile;
+    if (c.base >= V) {
+      c.base = 0;
+      if (++c.q == rows_req) { c.q = 0; ++c.req; }
+      set_row(c);
+    }
+  };
+  TileCursor cur;
+  {
+    const int rg = t0 / tpr;
+    cur.base = (t0 - rg * tpr) * kTile;
+    cur.req = rg / rows_req;
+    cur.q = rg - cur.req * rows_req;
+    set_row(cur);
+  }
+
+  // publish a row's folded key; count a request's finished tiles, the last warp runs the cut
+  auto flush_key = [&](int slot, uint64_t key) {
+    if (lane == 0 && key) atomicMax(reinterpret_cast<unsigned long long*>(P.keys) + slot, key);
+  };
+  auto flush_count = [&](int req, int cnt) {
+    if (!P.fused_cut) return;
+    int old = 0;
+    if (lane == 0) {   // release: this lane's key updates precede the count; acquire: others' too
+      asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(P.counters + req), "r"(cnt) : "memory");
+    }
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old + cnt == tiles_req) {                      // this warp finished request `req`
+      __syncwarp();
+      __threadfence();
+      const int d = P.depth ? min(max(P.depth[req], 0), K) : K;
+      cut_request(req, d, true, P.stats_only != 0, nullptr, P.keys, P.drows > 0, true, P.rows_t, K, V,
+                  P.tokens, nullptr, P.out_tokens, P.out_accepted, P.out_alpha, P.out_cum, P.out_E,
+                  P.status, lane);
+      if (lane == 0) P.counters[req] = 0;
     }
   };
 
-  TileRegs<BF16> cur, nxt;
-  const uint8_t* row = nullptr;
-  int base = 0;
-  size_t slot = 0;
-  long long t = gw;
-  if (t < P.total_tiles) {
-    locate(t, row, base, slot);
-    if (P.aligned) load_tile<BF16>(cur, row, base, V, lane);
-  }
-  while (t < P.total_tiles) {
-    const long long tn = t + nwarps;
-    const uint8_t* nrow = nullptr;
-    int nbase = 0;
-    size_t nslot = 0;
-    if (tn < P.total_tiles) {                  // prefetch the next tile while this one is scanned
-      locate(tn, nrow, nbase, nslot);
-      if (P.aligned) load_tile<BF16>(nxt, nrow, nbase, V, lane);
+  int acc_slot = cur.slot, acc_req = cur.req, acc_cnt = 0;
+  uint64_t acc_key = 0;
+  for (int t = t0; t < t1; ++t) {
+    uint64_t key;
+    if (P.aligned) {                                   // 16-byte loads; the other resident warps hide them
+      TileRegs<BF16> a;
+      load_tile<BF16>(a, cur.row, cur.base, V, lane);
+      key = tile_key_regs<BF16>(a, cur.base, lane);
+    } else {
+      key = tile_key_scalar<BF16>(cur.row, cur.base, V, lane);
     }
-    uint64_t key = tile_key<BF16>(cur, row, base, V, lane, P.aligned != 0);
-    key = warp_max_u64(key);
-    if (lane == 0 && key) atomicMax(reinterpret_cast<unsigned long long*>(P.keys) + slot, key);
-    cur = nxt;
-    row = nrow;
-    base = nbase;
-    slot = nslot;
-    t = tn;
+    if (cur.slot != acc_slot) {
+      flush_key(acc_slot, acc_key);
+      acc_slot = cur.slot;
+      acc_key = key;
+    } else {
+      acc_key = key > acc_key ? key : acc_key;
+    }
+    if (cur.req != acc_req) {
+      flush_count(acc_req, acc_cnt);
+      acc_req = cur.req;
+      acc_cnt = 1;
+    } else {
+      ++acc_cnt;
+    }
+    step(cur);
   }
+  flush_key(acc_slot, acc_key);
+  flush_count(acc_req, acc_cnt);
 }
 
 }  // namespace sv

@@ -134,9 +134,10 @@ cudaError_t launch_cut(const BudgetParams& p, const int32_t* depth, cudaStream_t
   return launch_pdl(reinterpret_cast<const void*>(&cut_kernel), grid, kCutThreads, 0, stream, args);
 }
 
-cudaError_t argmax_blocks_per_sm(bool bf16, int* out) {
+cudaError_t argmax_blocks_per_sm(bool bf16, int nstage, int* out) {
   const void* fn = bf16 ? reinterpret_cast<const void*>(&argmax_kernel<true>)
                         : reinterpret_cast<const void*>(&argmax_kernel<false>);
+  (void)nstage;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, fn, 256, 0);
 }
 
@@ -145,10 +146,11 @@ cudaError_t launch_argmax(bool bf16, const ArgmaxParams& p, int grid, cudaStream
   void* args[] = {&q};
   const void* fn = bf16 ? reinterpret_cast<const void*>(&argmax_kernel<true>)
                         : reinterpret_cast<const void*>(&argmax_kernel<false>);
-  // the previous call's cut kernel cleared the keys this grid folds into: plain stream order
+  // the previous call cleared the keys and counters this grid folds into: plain stream order
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   return cudaLaunchKernelExC(&cfg, fn, args);
 }

@@ -163,6 +163,11 @@ __device__ __forceinline__ int warp_draw(MassFn mass, float cum0, float t, int w
   return ((warp * kNV + js) * 32 + l) * kChunk + es;
 }
 
+// lane 0 of each warp loads the drafted token; every lane needs to know whether it was in range
+__device__ __forceinline__ bool xin_all(bool xin_lane0) {
+  return __shfl_sync(0xffffffffu, xin_lane0 ? 1 : 0, 0) != 0;
+}
+
 template <bool BF16, int NT>
 __global__ void __launch_bounds__(NT, (NT <= 256) ? 2 : 1) sample_kernel(const __grid_constant__ RowParams P) {
   constexpr int NW = NT / 32;
@@ -251,10 +256,16 @@ __global__ void __launch_bounds__(NT, (NT <= 256) ? 2 : 1) sample_kernel(const _
       mbar_arrive_tx(x1, static_cast<uint32_t>(nent) * 16u);
       if (pair) mbar_arrive_tx(x2, static_cast<uint32_t>(nent) * 4u);
     }
+    // the draws this unit may need: the bonus draw from p only at the request's verified depth
+    // (or at every row when the depth is chosen after this kernel); the residual only where the
+    // accept test fails (decided below from the merged normalisers, as the cut kernel will)
     const float uK = stats_only ? 0.f : P.uniforms[static_cast<size_t>(b) * (K + 1) + K];
+    const float uk = (stats_only || k >= K) ? 0.f : P.uniforms[static_cast<size_t>(b) * (K + 1) + k];
+    const int dep = P.depth ? min(max(P.depth[b], 0), K) : K;
+    const bool pdraw_here = !stats_only && ((P.flags & F_ALL_PDRAWS) != 0 || k == dep);
     float ztx = 0.f, zdx = 0.f;
     bool xin = false;
-    if (!stats_only && rank == 0 && tid == 0 && k < K) {
+    if (!stats_only && k < K && lane == 0) {
       const int x = P.tokens[static_cast<size_t>(b) * K + k];
       xin = (x >= 0 && x < V);
       if (xin) {
@@ -397,6 +408,15 @@ __global__ void __launch_bounds__(NT, (NT <= 256) ? 2 : 1) sample_kernel(const _
     Ptot = warp_sum(Ptot);
     const float at = ex2((mt - Mt) * c) * inv_St;       // p_v = e_v * at for this warp's logits
     const float ad = pair ? ex2((md - Md) * c) / Sd : 0.f;
+    // p_k(x_k), q_k(x_k) and the accept test, bitwise as the cut kernel will evaluate it
+    float px = 0.f, qx = 0.f;
+    if (lane == 0 && xin) {
+      px = ex2(fmaf(ztx, c, -Mt * c)) * inv_St;
+      qx = ex2(fmaf(zdx, c, -Md * c)) / Sd;
+    }
+    px = __shfl_sync(0xffffffffu, px, 0);
+    qx = __shfl_sync(0xffffffffu, qx, 0);
+    const bool rejects = !stats_only && k < K && !(xin_all(xin) && uk * qx < px);
 
     // ---- 3. exchange #2: residual mass per warp
     float Rtot = 0.f, wr[EPL];
@@ -428,27 +448,27 @@ __global__ void __launch_bounds__(NT, (NT <= 256) ? 2 : 1) sample_kernel(const _
     }
 
     // ---- 4. row record and inverse-CDF draws
+    const bool need_r = pair && rejects && Rtot > 0.f;
+    const bool need_p = pdraw_here || (rejects && !(Rtot > 0.f));   // p == q: the residual is empty
     int own_p = -1, own_r = -1;
     float cum_p = 0.f, cum_r = 0.f;
-    if (!stats_only) {
-      own_p = select_entry<EPL>(wp, 0.f, uK * Ptot, lane, &cum_p);
-      if (pair) own_r = select_entry<EPL>(wr, 0.f, uK * Rtot, lane, &cum_r);
-    }
+    if (need_p) own_p = select_entry<EPL>(wp, 0.f, uK * Ptot, lane, &cum_p);
+    if (need_r) own_r = select_entry<EPL>(wr, 0.f, uK * Rtot, lane, &cum_r);
     if (rank == 0 && tid == 0) {
       UnitRec* r = P.recs + u;
-      r->px = xin ? ex2(fmaf(ztx, c, -Mt * c)) * inv_St : 0.f;
-      r->qx = xin ? ex2(fmaf(zdx, c, -Md * c)) / Sd : 0.f;
+      r->px = px;
+      r->qx = qx;
       r->alpha = pair ? fminf(fmaxf(Ptot - Rtot, 0.f), 1.f) : 0.f;
       r->R = Rtot;
       if (own_p < 0) r->ps = -1;
       if (own_r < 0) r->rs = -1;
     }
     const int me = static_cast<int>(rank) * NW + warp;
-    if (own_p == me) {
+    if (need_p && own_p == me) {
       const int off = warp_draw([&](int j, int e) { return xt[j][e] * at; }, cum_p, uK * Ptot, warp, lane);
       if (lane == 0) P.recs[u].ps = lo + off;
     }
-    if (pair && own_r == me) {
+    if (need_r && own_r == me) {
       const int off = warp_draw([&](int j, int e) { return fmaxf(fmaf(xt[j][e], at, -xd[j][e] * ad), 0.f); },
                                 cum_r, uK * Rtot, warp, lane);
       if (lane == 0) P.recs[u].rs = lo + off;

@@ -12,6 +12,7 @@ constexpr int kNV = 4;            // chunks per thread per row
 constexpr int kMaxCluster = 16;   // CTAs that share one row (non-portable cluster size)
 constexpr int kMaxK = 31;         // drafted positions per request (lanes 0..K of one warp in the cut)
 constexpr int kTileLogits = 32 * kNV * kChunk;   // greedy path: logits per warp tile
+constexpr int kMaxArgmaxStages = 8;               // greedy path: staging ring depth limit
 
 // Status bits in the workspace's device status word.
 constexpr int kStatusTimeout = 1;
@@ -31,17 +32,32 @@ struct ArgmaxParams {
   const void* target;        // [B, K+1, V]
   const void* draft;         // [B, K, V] or null
   uint64_t* keys;            // [B, K+1, 2]
+  int32_t* counters;         // [B] finished tiles per request (zero between calls)
+  int32_t* status;
+  const int32_t* tokens;     // [B, K] (fused cut)
+  const int32_t* depth;      // [B] or null (fused cut)
+  int32_t* out_tokens;
+  int32_t* out_accepted;
+  float* out_alpha;
+  float* out_cum;
+  float* out_E;
   int B, K, V;
   int rows_t;                // target rows scanned per request (K+1, or K for overlap stats)
+  int drows;                 // draft rows scanned per request (K when the one-hot alpha is wanted)
   int tpr;                   // tiles per row
-  long long total_tiles;     // (B*rows_t + B*K*need_draft) * tpr
-  int aligned;               // rows start on 16-byte boundaries
+  long long total_tiles;     // B * (rows_t + drows) * tpr
+  int aligned;               // rows start on 16-byte boundaries (bulk-copy ring)
+  int nstage;                // ring depth (stages of 8 tiles)
+  long long wait_limit;      // polls per bounded wait; 0 = give up at once
+  int fused_cut;             // the warp that completes a request runs its cut
+  int stats_only;            // overlap statistics only (no tokens)
 };
 
 enum : int {
   F_NEED_DRAFT = 1,   // draft rows are read for positions k < K
   F_STATS_ONLY = 2,   // rows k < K only; alpha, no draws
   F_TMA = 8,          // rows are 16-byte aligned: bulk-copy staging ring
+  F_ALL_PDRAWS = 16,  // draw from p at every row (the verified depth is chosen afterwards)
 };
 
 struct RowParams {
@@ -90,7 +106,7 @@ struct BudgetParams {
 
 // Host-side launchers of the small kernels (defined next to them).
 cudaError_t launch_argmax(bool bf16, const ArgmaxParams& p, int grid, cudaStream_t stream);
-cudaError_t argmax_blocks_per_sm(bool bf16, int* out);
+cudaError_t argmax_blocks_per_sm(bool bf16, int nstage, int* out);
 cudaError_t launch_budget_cut(const BudgetParams& p, cudaStream_t stream);
 cudaError_t launch_cut(const BudgetParams& p, const int32_t* depth, cudaStream_t stream);
 

@@ -32,10 +32,12 @@
  *   Data errors found on the device (a draft token outside [0, V), a wait
  *   that ran out) are recorded in a status word inside the workspace and
  *   read with spec_get_status.
- * - The workspace (size from spec_workspace_bytes) holds the status word and
- *   per-row intermediate records.  Zero-fill it once before its first use
- *   (spec_workspace_init).  Calls that share a workspace must be ordered on
- *   one stream.
+ * - The workspace (at least spec_workspace_bytes) holds the status word,
+ *   per-row intermediate records and per-row argmax slots that every call
+ *   leaves zeroed.  Its layout depends only on ws_bytes: zero-fill it
+ *   (spec_workspace_init) before its first use and again whenever the same
+ *   buffer is passed with a different ws_bytes.  Calls that share a
+ *   workspace must be ordered on one stream.
  * - A call launches two kernels on `stream`: the row kernel and a small
  *   kernel (the serial cut, or the budget and the cut) chained to it with
  *   programmatic dependent launch.
@@ -189,6 +191,8 @@ void spec_debug_set_wait_limit(long long polls);
  * clusters, slice, stages, ring bytes, flags}.
  */
 void spec_debug_set_plan(int threads, int cluster, int nstage);
+/* Greedy-path schedule variant: bit 1 runs the cut in a separate kernel (0 = fused, default). */
+void spec_debug_set_variant(int variant);
 void spec_debug_last_plan(int32_t* out8);
 
 #ifdef __cplusplus

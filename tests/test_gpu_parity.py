@@ -152,7 +152,7 @@ def test_disjoint_supports_reject_at_zero(sv):
     w = W.Workload("disjoint", t, d, x, u, 1.0)
     out = _run_block(sv, w)
     assert np.all(out.accepted.cpu().numpy() == 0)
-    assert np.all(to_np(out.alpha) == 0.0)
+    np.testing.assert_allclose(to_np(out.alpha), 0.0, atol=1e-6)   # alpha = sum p - R carries fp32 rounding
     compare(out, oracle_verify(w), w)
 
 
