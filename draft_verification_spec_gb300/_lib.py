@@ -31,6 +31,8 @@ SIGNATURES = {
                                    c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "spec_alloc_budget": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p, c_size_t,
                                   c_void_p]),
+    "spec_verify_chain_greedy_static": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int, c_int,
+                                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "spec_debug_set_wait_limit": (None, [c_longlong]),
     "spec_debug_set_plan": (None, [c_int, c_int, c_int]),
     "spec_debug_last_plan": (None, [c_void_p]),

@@ -174,6 +174,37 @@ spec_status_t spec_alloc_budget(const float* alpha, int B, int K, int budget_N,
                                 void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Greedy (T == 0) chain verification that allocates nothing and needs no
+ * workspace.  The pages have no counterpart: this entry point exists for
+ * callers that cannot give the library device memory -- serving engines that
+ * reserve all device memory up front in their own pool and expose no
+ * allocator, and hosts that forbid cudaMalloc / cudaFree after start-up
+ * because those calls can synchronise the whole device.
+ *
+ * Same result as spec_verify_chain at temperature 0 (tokens, accepted
+ * counts, one-hot alpha when out_alpha is given; draft_logits needed only
+ * then).  Its scratch (status word, argmax slots, request counters) is one
+ * fixed device array of 80.25 KiB inside the library, held by every GPU that
+ * loads it until the process exits:
+ * - B * (K + 1) <= SPEC_STATIC_MAX_ROWS (4096), else SPEC_ERR_UNSUPPORTED;
+ * - the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture;
+ * - every call clears the parts it uses (cudaMemsetAsync) and shares the one
+ *   array, so calls that overlap on the GPU (other streams, other threads)
+ *   race: order them on one stream;
+ * - out_status (device int32, nullable) receives the raw status bits of the
+ *   call: 1 = a bounded wait ran out, 2 = a draft token outside [0, V).
+ * It calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define SPEC_STATIC_MAX_ROWS 4096
+spec_status_t spec_verify_chain_greedy_static(const void* target_logits, const void* draft_logits, int dtype,
+                                              const int32_t* tokens, int B, int K, int V,
+                                              const int32_t* depth, int32_t* out_tokens,
+                                              int32_t* out_accepted, float* out_alpha,
+                                              int32_t* out_status, void* stream);
+
+/*
  * Test hook: iteration limit of every bounded on-device wait (default
  * 1 << 22 polls).  0 makes every such wait give up at once, which sets
  * SPEC_ERR_DEVICE_TIMEOUT; in-flight copies are still drained with the
