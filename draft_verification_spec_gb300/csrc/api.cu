@@ -124,34 +124,32 @@ spec_status_t plan_rows(const void* target, const void* draft, int dtype, int B,
   const bool bf16 = dtype == SPEC_BF16;
   const bool greedy = T == 0.f;
   const int esz = bf16 ? 2 : 4;
-  int nt = V <= 256 * sv::kNV * sv::kChunk * sv::kMaxCluster ? 256 : 512;
-  if (g_force_nt.load()) nt = g_force_nt.load();
-  const int cap = nt * sv::kNV * sv::kChunk;
-  int cluster = (V + cap - 1) / cap;
+  // clusters of C CTAs, each streaming a slice of about 32768 logits per row in 4096-logit items
+  const int nt = 288;                       // 8 consumer warps + 1 producer warp
+  const int item = 4096;
+  int cluster = (V + 8 * item - 1) / (8 * item);
   if (g_force_cluster.load()) {
-    if (g_force_cluster.load() < cluster) return SPEC_ERR_UNSUPPORTED;
+    if (g_force_cluster.load() * 32 * item < V) return SPEC_ERR_UNSUPPORTED;
     cluster = g_force_cluster.load();
   }
   if (cluster > sv::kMaxCluster) return SPEC_ERR_UNSUPPORTED;
   int slice = (V + cluster - 1) / cluster;
   slice = static_cast<int>(align_up(slice, sv::kChunk));
+  if (slice > 32 * item) return SPEC_ERR_UNSUPPORTED;
   const bool tma = (static_cast<size_t>(V) * esz) % 16 == 0 && aligned16(target) &&
                    (!need_draft || aligned16(draft));
-  const int stage_row_bytes = static_cast<int>(align_up(static_cast<size_t>(slice) * esz, 128));
-  const size_t stage_bytes = static_cast<size_t>(need_draft ? 2 : 1) * stage_row_bytes;
-  int nstage = 0;
-  if (tma) {
-    const size_t budget = nt == 256 ? kRingBudgetSmall : kRingBudgetLarge;
-    nstage = static_cast<int>(budget / stage_bytes);
-    if (nstage > 4) nstage = 4;
-    if (nstage < 1) nstage = 1;
-    if (g_force_nstage.load() > 0 && g_force_nstage.load() <= 4) nstage = g_force_nstage.load();
-  }
+  const int stage_row_bytes = item * esz;
+  const size_t stage_bytes = 2 * static_cast<size_t>(stage_row_bytes);
+  // bf16: four 16 KB stages per CTA, three CTAs per SM; fp32: one CTA per SM
+  int nstage = bf16 ? 4 : static_cast<int>(kRingBudgetLarge / stage_bytes);
+  if (nstage > 6) nstage = 6;
+  if (nstage < 2) nstage = 2;
+  if (g_force_nstage.load() > 0 && g_force_nstage.load() <= 8) nstage = g_force_nstage.load();
   (void)greedy;
   plan->fn = bf16 ? sv::sample_kernel_bf16(nt) : sv::sample_kernel_f32(nt);
   plan->nt = nt;
   plan->cluster = cluster;
-  plan->smem = tma ? static_cast<size_t>(nstage) * stage_bytes : 0;
+  plan->smem = static_cast<size_t>(nstage) * stage_bytes;
   RowParams& p = plan->p;
   std::memset(&p, 0, sizeof(p));
   p.target = target;

@@ -13,6 +13,7 @@ constexpr int kMaxCluster = 16;   // CTAs that share one row (non-portable clust
 constexpr int kMaxK = 31;         // drafted positions per request (lanes 0..K of one warp in the cut)
 constexpr int kTileLogits = 32 * kNV * kChunk;   // greedy path: logits per warp tile
 constexpr int kMaxArgmaxStages = 8;               // greedy path: staging ring depth limit
+constexpr int kMaxStreamStages = 8;               // sampling path: staging ring depth limit
 
 // Status bits in the workspace's device status word.
 constexpr int kStatusTimeout = 1;

@@ -43,8 +43,8 @@
  *   programmatic dependent launch.
  * - Logits may contain -inf (probability 0); each row needs one finite
  *   value.  NaN / +inf give unspecified tokens (they are not scanned for).
- * - Limits: 1 <= V <= 262144, 0 <= K <= 31, B >= 0 (B == 0 is a no-op),
- *   T >= 0 and finite.
+ * - Limits: 1 <= V <= 262144 (fp32 logits at T > 0: V <= 131072),
+ *   0 <= K <= 31, B >= 0 (B == 0 is a no-op), T >= 0 and finite.
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
