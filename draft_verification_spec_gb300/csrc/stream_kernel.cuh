@@ -26,7 +26,7 @@
 
 #include <cuda_bf16.h>
 
-#include "spec_device.cuh"
+#include "spec_async.cuh"
 
 namespace sv {
 
