@@ -252,10 +252,16 @@ def last_plan() -> dict:
     return dict(zip(keys, list(buf)))
 
 
-def set_wait_limit(polls: int):
-    """Test hook: iteration limit of the kernels' bounded waits (-1 restores the default)."""
-    lib().spec_debug_set_wait_limit(int(polls))
+def set_variant(variant: int = 0):
+    """Test hook, greedy path: bit 1 runs the cut in its own kernel (0 = fused into the argmax kernel)."""
+    lib().spec_debug_set_variant(int(variant))
+
+
+def set_wait_limit(limit_us: int):
+    """Test hook: wall-time limit in microseconds of the kernels' bounded waits (0 = give up at
+    once, -1 restores the default of 200 ms)."""
+    lib().spec_debug_set_wait_limit(int(limit_us))
 
 
 __all__ = ["verify_chain", "verify_block", "overlap_alpha", "alloc_budget", "Workspace", "VerifyOutput",
-           "SpecError", "set_wait_limit", "set_plan", "last_plan", "lib"]
+           "SpecError", "set_wait_limit", "set_plan", "set_variant", "last_plan", "lib"]

@@ -21,13 +21,12 @@ using sv::BudgetParams;
 using sv::RowParams;
 using sv::UnitRec;
 
-constexpr long long kDefaultWaitLimit = 1ll << 22;
+constexpr long long kDefaultWaitLimit = 200000000ll;   // ns of wall time per bounded on-device wait
 std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
 
 constexpr size_t kAlign = 256;
 constexpr int kMaxV = 262144;
 constexpr int kBudgetMaxKeys = 8192;
-constexpr size_t kRingBudgetSmall = 100 * 1024;   // per CTA when two CTAs share an SM
 constexpr size_t kRingBudgetLarge = 200 * 1024;   // per CTA when one CTA fills an SM
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -119,18 +118,62 @@ struct RowPlan {
 };
 
 // Chooses threads per CTA, cluster size, slice and staging depth for a (dtype, V) pair.
+// Resident CTAs of the row kernel on this device (SMs x CTAs per SM), cached per kernel and size.
+std::map<std::tuple<int, const void*, size_t>, int> g_resident;
+cudaError_t resident_ctas(const void* fn, int nt, size_t smem, int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_resident.find(std::make_tuple(dev, fn, smem));
+    if (it != g_resident.end()) {
+      *out = it->second;
+      return cudaSuccess;
+    }
+  }
+  e = prepare_kernel(dev, fn);
+  if (e != cudaSuccess) return e;
+  int sms = 0, per_sm = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, nt, smem);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_resident[std::make_tuple(dev, fn, smem)] = sms * per_sm;
+  *out = sms * per_sm;
+  return cudaSuccess;
+}
+
 spec_status_t plan_rows(const void* target, const void* draft, int dtype, int B, int K, int V,
                         float T, bool need_draft, bool stats_only, RowPlan* plan) {
   const bool bf16 = dtype == SPEC_BF16;
   const bool greedy = T == 0.f;
   const int esz = bf16 ? 2 : 4;
-  // clusters of C CTAs, each streaming a slice of about 32768 logits per row in 4096-logit items
-  const int nt = 288;                       // 8 consumer warps + 1 producer warp
+  // clusters of C CTAs, each CTA streaming a slice of V / C logits per row in 4096-logit items
+  const int nt = 256;                       // 8 warps, each thread streaming its own chunks
   const int item = 4096;
-  int cluster = (V + 8 * item - 1) / (8 * item);
+  const void* fn = bf16 ? sv::sample_kernel_bf16(nt) : sv::sample_kernel_f32(nt);
+  const int units = B * (stats_only ? K : K + 1);
+  int cluster = 0;
   if (g_force_cluster.load()) {
     if (g_force_cluster.load() * 32 * item < V) return SPEC_ERR_UNSUPPORTED;
     cluster = g_force_cluster.load();
+  } else {
+    // The kernel is issue-bound and a unit's CTAs work in lockstep.  Split rows across more CTAs
+    // while each slice keeps at least 7 items (so per-unit exchanges stay small against the
+    // streaming) and there are at most 2.5 CTA-tasks (units x C) per resident CTA slot (beyond
+    // that the extra per-unit rounds cost more than the finer balance gains).  A slice holds at
+    // most 32 items.
+    int slots = 0;
+    if (resident_ctas(fn, nt, 2 * static_cast<size_t>(item) * esz * sv::kStreamStagesHost, &slots) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    const int cmin = (V + 32 * item - 1) / (32 * item);
+    cluster = 1;
+    while (cluster * 2 <= sv::kMaxCluster && static_cast<long long>(V) >= 2ll * cluster * 7 * item &&
+           static_cast<long long>(units) * cluster * 2 * 2 <= 5ll * slots)
+      cluster *= 2;
+    while (cluster < cmin) cluster *= 2;
   }
   if (cluster > sv::kMaxCluster) return SPEC_ERR_UNSUPPORTED;
   int slice = (V + cluster - 1) / cluster;
@@ -140,13 +183,11 @@ spec_status_t plan_rows(const void* target, const void* draft, int dtype, int B,
                    (!need_draft || aligned16(draft));
   const int stage_row_bytes = item * esz;
   const size_t stage_bytes = 2 * static_cast<size_t>(stage_row_bytes);
-  // bf16: four 16 KB stages per CTA, three CTAs per SM; fp32: one CTA per SM
-  int nstage = bf16 ? 4 : static_cast<int>(kRingBudgetLarge / stage_bytes);
-  if (nstage > 6) nstage = 6;
-  if (nstage < 2) nstage = 2;
-  if (g_force_nstage.load() > 0 && g_force_nstage.load() <= 8) nstage = g_force_nstage.load();
+  // the kernel's copy pipeline is kStreamStages items deep: bf16 64 KB per CTA (three CTAs per
+  // SM), fp32 128 KB (one CTA per SM)
+  const int nstage = sv::kStreamStagesHost;
   (void)greedy;
-  plan->fn = bf16 ? sv::sample_kernel_bf16(nt) : sv::sample_kernel_f32(nt);
+  plan->fn = fn;
   plan->nt = nt;
   plan->cluster = cluster;
   plan->smem = static_cast<size_t>(nstage) * stage_bytes;
@@ -202,10 +243,6 @@ bool bad_T(float T) { return !(T >= 0.f) || std::isinf(T); }
 
 // Greedy path: the streaming argmax kernel over target rows (and draft rows when need_draft).
 // Ring: stages of 8 tiles (16 KB bf16 / 32 KB fp32); about 64 KB per CTA.
-int argmax_stages(int dtype) {
-  if (g_force_nstage.load() > 0) return g_force_nstage.load() > 8 ? 8 : g_force_nstage.load();
-  return dtype == SPEC_BF16 ? 4 : 2;
-}
 std::map<int, int> g_argmax_grid;
 spec_status_t launch_greedy(const void* target, const void* draft, int dtype, int B, int K, int V,
                             bool need_draft, bool stats_only, bool fused_cut, uint64_t* keys,
@@ -215,13 +252,13 @@ spec_status_t launch_greedy(const void* target, const void* draft, int dtype, in
   int grid_cap;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    const int gkey = dev * 64 + (dtype == SPEC_BF16) * 16 + argmax_stages(dtype);
+    const int gkey = dev * 2 + (dtype == SPEC_BF16);
     auto it = g_argmax_grid.find(gkey);
     if (it == g_argmax_grid.end()) {
       int sms = 0, per_sm = 0;
       if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SPEC_ERR_CUDA;
       // one wave of resident CTAs (the bf16 and fp32 instances differ only in registers)
-      if (sv::argmax_blocks_per_sm(dtype == SPEC_BF16, argmax_stages(dtype), &per_sm) != cudaSuccess)
+      if (sv::argmax_blocks_per_sm(dtype == SPEC_BF16, 0, &per_sm) != cudaSuccess)
         return SPEC_ERR_CUDA;
       g_argmax_grid[gkey] = sms * (per_sm > 0 ? per_sm : 1);
       it = g_argmax_grid.find(gkey);
@@ -244,12 +281,13 @@ spec_status_t launch_greedy(const void* target, const void* draft, int dtype, in
   const int variant = g_variant.load();
   p.fused_cut = fused_cut && !(variant & 2);
   p.stats_only = stats_only;
-  p.nstage = argmax_stages(dtype);
   p.wait_limit = g_wait_limit.load();
   const int esz = dtype == SPEC_BF16 ? 2 : 4;
   p.aligned = (static_cast<size_t>(V) * esz) % 16 == 0 && aligned16(target) && (!need_draft || aligned16(draft));
-  const long long warps_needed = p.total_tiles;
-  long long grid = (warps_needed + 7) / 8;
+  // every warp takes the same number of tiles (the fewest one resident wave allows), so no
+  // warp is left with an extra tile after the others finish
+  const long long per_warp = (p.total_tiles + 8ll * grid_cap - 1) / (8ll * grid_cap);
+  long long grid = (p.total_tiles + 8 * per_warp - 1) / (8 * per_warp);
   if (grid > grid_cap) grid = grid_cap;
   if (grid < 1) grid = 1;
   if (sv::launch_argmax(dtype == SPEC_BF16, p, static_cast<int>(grid), stream) != cudaSuccess) return SPEC_ERR_CUDA;
@@ -515,14 +553,14 @@ spec_status_t spec_alloc_budget(const float* alpha, int B, int K, int budget_N, 
                                                                                       : SPEC_ERR_CUDA;
 }
 
-void spec_debug_set_wait_limit(long long polls) {
-  g_wait_limit.store(polls < 0 ? kDefaultWaitLimit : polls);
+void spec_debug_set_wait_limit(long long limit_us) {
+  g_wait_limit.store(limit_us < 0 ? kDefaultWaitLimit : limit_us * 1000);
 }
 
 void spec_debug_set_plan(int threads, int cluster, int nstage) {
   g_force_nt.store(threads == 256 || threads == 512 ? threads : 0);
   g_force_cluster.store(cluster > 0 && cluster <= sv::kMaxCluster ? cluster : 0);
-  g_force_nstage.store(nstage > 0 && nstage <= 4 ? nstage : 0);
+  g_force_nstage.store(nstage > 0 && nstage <= 16 ? nstage : 0);
 }
 
 void spec_debug_set_variant(int variant) { g_variant.store(variant & 3); }

@@ -235,6 +235,9 @@ __global__ void __launch_bounds__(256, BF16 ? 4 : 2) argmax_kernel(const __grid_
     }
   };
 
+  // launched with programmatic serialization: everything above is index arithmetic; the logits,
+  // keys and counters are touched only once the preceding grid has completed and flushed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   int acc_slot = cur.slot, acc_req = cur.req, acc_cnt = 0;
   uint64_t acc_key = 0;
   for (int t = t0; t < t1; ++t) {

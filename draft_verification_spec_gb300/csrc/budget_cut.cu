@@ -146,12 +146,18 @@ cudaError_t launch_argmax(bool bf16, const ArgmaxParams& p, int grid, cudaStream
   void* args[] = {&q};
   const void* fn = bf16 ? reinterpret_cast<const void*>(&argmax_kernel<true>)
                         : reinterpret_cast<const void*>(&argmax_kernel<false>);
-  // the previous call cleared the keys and counters this grid folds into: plain stream order
+  // programmatic dependent launch: the grid may be scheduled while the preceding kernel drains;
+  // it waits (griddepcontrol.wait) for that kernel's completion before its first memory access
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(256, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 

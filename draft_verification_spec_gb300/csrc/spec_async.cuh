@@ -1,5 +1,5 @@
-// PTX wrappers for thread-block clusters, DSMEM, mbarriers and bulk (TMA) copies -- sm_90+
-// forms, compiled for sm_103a -- used by the streaming row kernel.
+// PTX wrappers for thread-block clusters, DSMEM stores and mbarriers (sm_90+ forms, compiled
+// for sm_103a), used by the streaming row kernel's cluster exchanges.
 #pragma once
 
 #include <cstdint>
@@ -44,17 +44,6 @@ __device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_peer_v4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
-}
-__device__ __forceinline__ void st_peer_v4u(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                            uint32_t d) {
-  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
-               "r"(c), "r"(d)
-               : "memory");
-}
 
 // Asynchronous stores into a peer CTA's shared memory; completion is counted (in bytes) on the
 // peer's mbarrier, so the receiver needs no fence and no cluster barrier.
@@ -71,7 +60,7 @@ __device__ __forceinline__ void st_async_f32(uint32_t addr, float a, uint32_t ba
                : "memory");
 }
 
-// ---------------------------------------------------------------- mbarrier + bulk copy
+// ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
@@ -82,17 +71,15 @@ __device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
-// One poll of a phase; the thread may be suspended up to kWaitSliceNs inside it instead of
-// spinning, which leaves issue slots to the warps that have work.
-constexpr uint32_t kWaitSliceNs = 20000;
+// One poll of a phase (the hardware may hold the thread briefly before answering).
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "n"(kWaitSliceNs)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
@@ -101,39 +88,33 @@ __device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) 
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "n"(kWaitSliceNs)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity, long long limit) {
-  for (long long i = 0; i < limit; ++i)
-    if (mbar_try_cluster(bar, parity)) return true;
-  return false;
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
 }
-// Bounded wait for the phase with this parity; false if `limit` polls ran out (limit 0: at once).
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit) {
-  if (limit <= 0) return false;
-  for (long long i = 0; i < limit; ++i)
-    if (mbar_try(bar, parity)) return true;
-  return false;
+// Bounded waits for the phase with this parity: false once `limit_ns` nanoseconds of wall time
+// have passed without it (limit 0: give up at once).  The clock is read every 16 polls.
+template <bool CLUSTER>
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, long long limit_ns) {
+  if (limit_ns <= 0) return false;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+#pragma unroll 1
+    for (int k = 0; k < 16; ++k)
+      if (CLUSTER ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
+    if (static_cast<long long>(global_ns() - t0) > limit_ns) return false;
+  }
 }
-// Global -> shared bulk copy (16-byte aligned addresses, size a multiple of 16),
-// completion counted on the mbarrier; the L2 is told the source is read once.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
-      : "memory");
-}
-__device__ __forceinline__ uint64_t l2_evict_first_policy() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity, long long limit_ns) {
+  return mbar_wait_for<true>(bar, parity, limit_ns);
 }
 
 }  // namespace sv

@@ -1,5 +1,5 @@
 // Device helpers shared by every kernel: exp2, warp reductions, argmax keys, and the
-// per-request cut.  The cluster / mbarrier / bulk-copy wrappers live in spec_async.cuh.
+// per-request cut.  The cluster / DSMEM / mbarrier wrappers live in spec_async.cuh.
 #pragma once
 
 #include <cstdint>

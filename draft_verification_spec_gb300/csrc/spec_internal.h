@@ -12,8 +12,7 @@ constexpr int kNV = 4;            // chunks per thread per row
 constexpr int kMaxCluster = 16;   // CTAs that share one row (non-portable cluster size)
 constexpr int kMaxK = 31;         // drafted positions per request (lanes 0..K of one warp in the cut)
 constexpr int kTileLogits = 32 * kNV * kChunk;   // greedy path: logits per warp tile
-constexpr int kMaxArgmaxStages = 8;               // greedy path: staging ring depth limit
-constexpr int kMaxStreamStages = 8;               // sampling path: staging ring depth limit
+constexpr int kStreamStagesHost = 4;              // sampling path: items in each thread's copy pipeline
 
 // Status bits in the workspace's device status word.
 constexpr int kStatusTimeout = 1;
@@ -48,8 +47,7 @@ struct ArgmaxParams {
   int tpr;                   // tiles per row
   long long total_tiles;     // B * (rows_t + drows) * tpr
   int aligned;               // rows start on 16-byte boundaries (bulk-copy ring)
-  int nstage;                // ring depth (stages of 8 tiles)
-  long long wait_limit;      // polls per bounded wait; 0 = give up at once
+  long long wait_limit;      // ns of wall time per bounded wait; 0 = give up at once
   int fused_cut;             // the warp that completes a request runs its cut
   int stats_only;            // overlap statistics only (no tokens)
 };
@@ -78,11 +76,11 @@ struct RowParams {
   int U;                     // rows (units) per request: K+1, or K in stats-only mode
   int total_units;           // B * U
   int slice;                 // logits per CTA slice (multiple of kChunk)
-  int nstage;                // staging ring depth (TMA path)
+  int nstage;                // copy pipeline depth in items (aligned rows)
   int stage_row_bytes;       // bytes per row slot in a stage (multiple of 128)
   int flags;
   float c;                   // log2(e) / T  (T > 0)
-  long long wait_limit;      // polls per bounded wait; 0 = give up at once
+  long long wait_limit;      // ns of wall time per bounded wait; 0 = give up at once
 };
 
 struct BudgetParams {

@@ -105,7 +105,7 @@ extern "C" spec_status_t spec_verify_chain_greedy_static(const void* target_logi
   const int esz = dtype == SPEC_BF16 ? 2 : 4;
   p.aligned = (static_cast<size_t>(V) * esz) % 16 == 0 && aligned16(target_logits) &&
               (!need_draft || aligned16(draft_logits));
-  p.wait_limit = 1ll << 22;
+  p.wait_limit = 200000000ll;   // ns (this kernel has no waits)
   p.fused_cut = 1;
   p.stats_only = 0;
   long long grid = (p.total_tiles + 7) / 8;

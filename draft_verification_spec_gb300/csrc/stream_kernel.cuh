@@ -2,21 +2,23 @@
 //
 // A thread-block cluster of C CTAs works on one unit at a time -- target row k and, for k < K,
 // draft row k -- looping over units (persistent).  CTA r owns the vocabulary slice
-// [r*slice, (r+1)*slice) of every row and streams it in items of 4096 logits per row through a
-// shared-memory ring: a producer warp issues one-thread bulk copies into free stages (full /
-// empty mbarriers), eight consumer warps read them.  Inside an item, consumer warp w owns logits
-// [w*512, (w+1)*512), lane-interleaved in 8-logit chunks.
+// [r*slice, (r+1)*slice) of every row and walks it in items of 4096 logits per row.  Inside an
+// item, warp w owns logits [w*512, (w+1)*512), lane-interleaved in 8-logit chunks, and every
+// thread fetches its own chunks with 16-byte cp.async copies into its own shared-memory slots,
+// kStreamStages - 1 items ahead of the one it computes on, across pass and unit boundaries: no
+// producer warp and no CTA-wide staging barrier.
 //
 // Per unit:
-//   pass 1 (from HBM, kept in L2 with an evict-last hint): per-thread online (max, sum of
+//   pass 1 (from HBM): per-thread online (max, sum of
 //     2^((z - m) c)) of the target and draft rows -> warp partials -> exchange #1 with st.async
 //     into every CTA of the cluster, completing on its mbarrier -> the row's normalisers of p and
 //     q, merged in one fixed order so every warp of every CTA holds bitwise-identical values;
 //     p_k(x_k), q_k(x_k) and the accept test, as the cut kernel will evaluate them
-//   pass 2 (the same bytes again, now L2 hits, evict-first): per element p = 2^(z c - offt),
+//   pass 2 (the same bytes again, L2 hits while the data streamed in between fits in L2): per element p = 2^(z c - offt),
 //     q = 2^(z c - offd); per (item, warp) masses of r = max(0, p - q) and of p -> CTA totals ->
 //     exchange #2 -> residual mass R, alpha = sum p - R (= sum min(p, q)), and the owner of each
-//     needed inverse-CDF draw, found in vocabulary order (CTA, item, warp)
+//     needed inverse-CDF draw, found in vocabulary order (CTA, item, warp).  A pair that passes
+//     the test and draws nothing only needs alpha = sum 2^min(a, b) (one exp2 per logit pair).
 //   the owner warp reloads its 512 logits of the row(s) and walks slot / lane / element prefix
 //     sums to the drawn index.  The residual is drawn only where the test fails, the p draw only
 //     at the verified depth (or at every row when the depth is chosen afterwards).
@@ -30,24 +32,13 @@
 
 namespace sv {
 
-constexpr int kStreamWarps = 8;                                 // consumer warps
-constexpr int kStreamThreads = 32 * (kStreamWarps + 1);         // + the producer warp
+constexpr int kStreamWarps = 8;                                 // warps per CTA
+constexpr int kStreamThreads = 32 * kStreamWarps;
+constexpr int kStreamStages = kStreamStagesHost;                // items in each thread's cp.async pipeline
 constexpr int kStreamNV = 2;                                    // 8-logit chunks per lane per item
 constexpr int kStreamWarpSpan = 32 * kStreamNV * kChunk;        // logits of one warp per item (512)
 constexpr int kStreamItem = kStreamWarps * kStreamWarpSpan;     // logits per row per item (4096)
 constexpr int kStreamMaxItems = 32;                             // items per slice (slice <= 131072)
-
-template <bool BF16>
-__device__ __forceinline__ float chunk_elem(const uint4 (&w)[BF16 ? 1 : 2], int e) {   // logit e of a chunk
-  if constexpr (BF16) {
-    const uint32_t word = (e < 2) ? w[0].x : (e < 4) ? w[0].y : (e < 6) ? w[0].z : w[0].w;
-    return __uint_as_float((e & 1) ? (word & 0xffff0000u) : (word << 16));
-  } else {
-    const uint4 v = w[e >> 2];
-    const uint32_t word = ((e & 3) == 0) ? v.x : ((e & 3) == 1) ? v.y : ((e & 3) == 2) ? v.z : v.w;
-    return __uint_as_float(word);
-  }
-}
 
 __device__ __forceinline__ float lg2f(float x) {
   float y;
@@ -81,20 +72,23 @@ __device__ __forceinline__ uint64_t pair_of(const uint32_t* w, int i) {
   else return pk(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1]));
 }
 
-__device__ __forceinline__ uint64_t l2_evict_last_policy() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
 
-// Named barrier among the consumer warps (the producer warp never joins it).
+// Every warp of the CTA.
 __device__ __forceinline__ void consumers_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(32 * kStreamWarps) : "memory");
 }
+
+// 16-byte asynchronous global -> shared copy by this thread (L1 bypassed), `src_bytes` <= 16 of
+// them read from global and the rest of the 16 zero-filled; completion tracked per commit group.
+// (No L2 cache-policy operand: the form carrying both a source size and a cache policy faulted.)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // First entry (vocabulary order: lane-major, EPL entries per lane) whose running prefix
 // cum0 + sum(..) crosses t; if rounding leaves none, the last entry with positive mass; -1 if
@@ -141,15 +135,15 @@ __global__ void __launch_bounds__(kStreamThreads, BF16 ? 3 : 1) stream_kernel(co
   constexpr int NW = kStreamWarps;
   constexpr int ENT = kMaxCluster * NW;   // exchange #1 entries per row: (CTA c, warp w) at c*NW + w
   constexpr int EPL = ENT / 32;
-  constexpr int ITEM_BYTES = kStreamItem * ESZ;   // one row of one item in the ring
+  constexpr int EP = kStreamMaxItems * NW / 32;   // (item, warp) entries per lane in the owner search
   using Chunk = uint4[BF16 ? 1 : 2];
 
-  extern __shared__ __align__(128) uint8_t ring[];            // [nstage][2 rows][ITEM_BYTES]
+  // each thread's own copies: stage s, row r, chunk j, 16-byte piece h of (warp, lane) at uint4
+  // index (((s * 2 + r) * NV + j) * HP + h) * 256 + warp * 32 + lane (a warp reads 512 B at once)
+  extern __shared__ __align__(128) uint4 stage_buf[];
   __shared__ __align__(16) float4 mbox1[2][ENT];               // (m_t, s_t, m_d, s_d) per (CTA, warp)
   __shared__ __align__(16) float2 mbox2[2][kMaxCluster];       // (R, P) per CTA
   __shared__ float2 part[2][kStreamMaxItems][NW];              // (R, P) per (item, warp) of this CTA
-  __shared__ __align__(8) uint64_t full_bar[kMaxStreamStages];
-  __shared__ __align__(8) uint64_t empty_bar[kMaxStreamStages];
   __shared__ __align__(8) uint64_t x1_bar[2];
   __shared__ __align__(8) uint64_t x2_bar[2];
 
@@ -165,7 +159,6 @@ __global__ void __launch_bounds__(kStreamThreads, BF16 ? 3 : 1) stream_kernel(co
   const bool stats_only = (P.flags & F_STATS_ONLY) != 0;
   const bool all_pdraws = (P.flags & F_ALL_PDRAWS) != 0;
   const float c = P.c;
-  const int nstage = P.nstage;
   const int nent = static_cast<int>(C) * NW;
   const int nunits = static_cast<int>(cid) < P.total_units
                          ? (P.total_units - static_cast<int>(cid) + static_cast<int>(ncl) - 1) / static_cast<int>(ncl)
@@ -186,10 +179,6 @@ __global__ void __launch_bounds__(kStreamThreads, BF16 ? 3 : 1) stream_kernel(co
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
-    for (int s = 0; s < nstage; ++s) {
-      mbar_init(smem_addr(&full_bar[s]), 1);
-      mbar_init(smem_addr(&empty_bar[s]), NW);
-    }
     for (int p = 0; p < 2; ++p) {
       mbar_init(smem_addr(&x1_bar[p]), 1);
       mbar_init(smem_addr(&x2_bar[p]), 1);
@@ -199,80 +188,116 @@ __global__ void __launch_bounds__(kStreamThreads, BF16 ? 3 : 1) stream_kernel(co
   __syncthreads();
   cluster_sync();   // every CTA's barriers exist before any peer sends into them
 
-  if (warp == NW) {
-    // ================= producer warp: stream (unit, pass, item) into the ring =================
-    if (tma && lane == 0) {
-      const uint64_t keep = l2_evict_last_policy(), drop = l2_evict_first_policy();
-      int slot = 0;                          // running item count
-      bool give_up = false;
-      for (int i = 0; i < nunits && !give_up; ++i) {
-        int u, b, k;
-        unit_of(i, u, b, k);
-        const bool pair = need_draft && k < K;
-        const int passes = needs_p2(pair, pdraw_row(b, k)) ? 2 : 1;
-        const uint8_t* rt = static_cast<const uint8_t*>(P.target) +
-                            ((static_cast<size_t>(b) * (K + 1) + k) * static_cast<size_t>(V) + lo) * ESZ;
-        const uint8_t* rd = static_cast<const uint8_t*>(P.draft) +
-                            ((static_cast<size_t>(b) * K + k) * static_cast<size_t>(V) + lo) * ESZ;
-        for (int pass = 0; pass < passes && !give_up; ++pass) {
-          for (int it = 0; it < nitems; ++it, ++slot) {
-            const int s = slot % nstage;
-            if (slot >= nstage &&            // stage s free once every consumer warp released it
-                !mbar_wait_bounded(smem_addr(&empty_bar[s]), ((slot / nstage) - 1) & 1, 1ll << 17)) {
-              atomicOr(P.status, kStatusTimeout);
-              give_up = true;
-              break;
-            }
-            const int e0 = it * kStreamItem;
-            const uint32_t bytes = static_cast<uint32_t>(min(kStreamItem, n - e0)) * ESZ;
-            const uint32_t bar = smem_addr(&full_bar[s]);
-            mbar_arrive_tx(bar, bytes * (pair ? 2u : 1u));
-            const uint64_t pol = pass == 0 ? keep : drop;
-            const uint32_t dst = smem_addr(ring) + s * 2 * ITEM_BYTES;
-            bulk_g2s(dst, rt + static_cast<size_t>(e0) * ESZ, bytes, bar, pol);
-            if (pair) bulk_g2s(dst + ITEM_BYTES, rd + static_cast<size_t>(e0) * ESZ, bytes, bar, pol);
-          }
-        }
-      }
-      // every copy issued is waited for by the consumers before they leave
-    }
-    cluster_sync_relaxed();
-    return;
-  }
-
-  // ======================= consumer warps =======================
-  bool tabort = false;   // a staged-data wait gave up once (test hook or a lost copy)
-  bool xabort = false;   // gave up waiting for an exchange
-  const long long xlimit = 1ll << 17;   // polls of up to kWaitSliceNs each
+  bool xabort = false;   // gave up waiting for an exchange (test hook or a lost peer)
+  const long long xlimit = P.wait_limit;   // ns per exchange wait; 0 gives up at once
   uint32_t x2ph = 0;
 
   constexpr uint32_t NEG = BF16 ? 0xff80ff80u : 0xff800000u;
   constexpr int WPC = BF16 ? 4 : 8;                  // 32-bit words per 8-logit chunk
   constexpr int IW = kStreamNV * WPC;                // words per lane per row per item
   constexpr int NP = kStreamNV * kChunk / 2;         // logit pairs per lane per row per item
-  // this lane's logits of item `it` of one row, as raw words: 16-byte reads from the ring, or
-  // element-wise reads (ragged slice end, unaligned rows) with -inf past the slice end
-  auto read_item = [&](uint32_t (&W)[IW], const uint8_t* st, const uint8_t* grow, int it) {
+  constexpr int NV = kStreamNV;
+  constexpr int HP = WPC / 4;                        // 16-byte pieces per 8-logit chunk
+  constexpr int S = kStreamStages;
+  // ---- per-thread copy pipeline over the CTA's (unit, pass, item) sequence, S - 1 items ahead;
+  // every step commits one group (possibly empty) so wait_group(S - 1) retires the oldest
+  int iu = 0, ipass = 0, iit = 0, ipasses = 0;       // issue cursor
+  bool ipair = false;
+  const uint8_t* irt = nullptr;
+  const uint8_t* ird = nullptr;
+  auto issue_unit = [&]() {
+    if (iu >= nunits) return;
+    int u, b, k;
+    unit_of(iu, u, b, k);
+    ipair = need_draft && k < K;
+    ipasses = needs_p2(ipair, pdraw_row(b, k)) ? 2 : 1;
+    irt = static_cast<const uint8_t*>(P.target) + ((static_cast<size_t>(b) * (K + 1) + k) * static_cast<size_t>(V) + lo) * ESZ;
+    ird = static_cast<const uint8_t*>(P.draft) + ((static_cast<size_t>(b) * K + k) * static_cast<size_t>(V) + lo) * ESZ;
+  };
+  int istage = 0;
+  auto issue_next = [&]() {
+    if (tma && iu < nunits && nitems > 0) {
+      const int e0 = iit * kStreamItem;
+      const int nval = min(kStreamItem, n - e0);
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        const int o = warp * kStreamWarpSpan + (j * 32 + lane) * kChunk;
+        const int vb = (nval - o) * ESZ;             // valid bytes from this chunk on
+#pragma unroll
+        for (int h = 0; h < HP; ++h) {
+          const int sb = min(max(vb - h * 16, 0), 16);
+          if (sb > 0) {
+            const size_t go = static_cast<size_t>(e0 + o) * ESZ + h * 16;
+            const int q = (((istage * 2) * NV + j) * HP + h) * 256 + warp * 32 + lane;
+            cp_async16(smem_addr(&stage_buf[q]), irt + go, static_cast<uint32_t>(sb));
+            if (ipair)
+              cp_async16(smem_addr(&stage_buf[q + NV * HP * 256]), ird + go, static_cast<uint32_t>(sb));
+          }
+        }
+      }
+      if (++iit == nitems) {
+        iit = 0;
+        if (++ipass == ipasses) {
+          ipass = 0;
+          ++iu;
+          issue_unit();
+        }
+      }
+    }
+    cp_async_commit();
+    if (++istage == S) istage = 0;
+  };
+  issue_unit();
+  for (int q = 0; q < S - 1; ++q) issue_next();
+  int stage = 0;   // stage of the next item to consume
+  // the next item of the sequence is in this thread's stage: issue the one S - 1 further on
+  // (into the stage consumed last step, whose words are already in registers), then retire it
+  auto next_item = [&]() {
+    issue_next();
+    cp_async_wait<S - 1>();
+  };
+  auto done_item = [&]() {
+    if (++stage == S) stage = 0;
+  };
+  // this lane's logits of item `it` of row r (0 target, 1 draft), as raw words: 16-byte reads
+  // of its own copies, -inf past the slice end; element-wise global reads for unaligned rows
+  auto read_item = [&](uint32_t (&W)[IW], int r, const uint8_t* grow, int it) {
     const int e0 = it * kStreamItem;
     const int nval = min(kStreamItem, n - e0);
-    if (tma && nval == kStreamItem) {
+    if (tma) {
 #pragma unroll
-      for (int j = 0; j < kStreamNV; ++j) {
-        const int o = warp * kStreamWarpSpan + (j * 32 + lane) * kChunk;
+      for (int j = 0; j < NV; ++j) {
 #pragma unroll
-        for (int h = 0; h < WPC / 4; ++h) {
-          const uint4 v = *reinterpret_cast<const uint4*>(st + o * ESZ + h * 16);
+        for (int h = 0; h < HP; ++h) {
+          const uint4 v = stage_buf[(((stage * 2 + r) * NV + j) * HP + h) * 256 + warp * 32 + lane];
           W[j * WPC + h * 4] = v.x;
           W[j * WPC + h * 4 + 1] = v.y;
           W[j * WPC + h * 4 + 2] = v.z;
           W[j * WPC + h * 4 + 3] = v.w;
         }
       }
+      if (nval < kStreamItem) {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+          const int o = warp * kStreamWarpSpan + (j * 32 + lane) * kChunk;
+#pragma unroll
+          for (int e = 0; e < kChunk; ++e) {
+            if (o + e >= nval) {
+              if constexpr (BF16) {
+                uint32_t& w = W[j * WPC + (e >> 1)];
+                w = (e & 1) ? ((w & 0x0000ffffu) | 0xff800000u) : ((w & 0xffff0000u) | 0x0000ff80u);
+              } else {
+                W[j * WPC + e] = NEG;
+              }
+            }
+          }
+        }
+      }
       return;
     }
-    const uint8_t* src = tma ? st : grow + static_cast<size_t>(e0) * ESZ;
+    const uint8_t* src = grow + static_cast<size_t>(e0) * ESZ;
 #pragma unroll
-    for (int j = 0; j < kStreamNV; ++j) {
+    for (int j = 0; j < NV; ++j) {
       const int o = warp * kStreamWarpSpan + (j * 32 + lane) * kChunk;
       const int nv = min(kChunk, max(0, nval - o));
 #pragma unroll
@@ -290,24 +315,6 @@ __global__ void __launch_bounds__(kStreamThreads, BF16 ? 3 : 1) stream_kernel(co
         }
       }
     }
-  };
-  // ring position of the next item, advanced without divisions
-  int stage = 0;
-  uint32_t fpar = 0;
-  // a wait that gives up (the test hook, or a lost copy) records the timeout, then still drains
-  // the copy with a long bound so no copy lands in a stage after it is reused or after exit
-  auto wait_item = [&]() {
-    if (!tma) return;
-    const uint32_t bar = smem_addr(&full_bar[stage]);
-    if (!tabort && mbar_wait_bounded(bar, fpar, P.wait_limit)) return;
-    if (!tabort) atomicOr(P.status, kStatusTimeout);
-    tabort = true;
-    if (!mbar_wait_bounded(bar, fpar, 1ll << 17)) atomicOr(P.status, kStatusTimeout);
-  };
-  auto release_item = [&]() {
-    __syncwarp();
-    if (tma && lane == 0) mbar_arrive(smem_addr(&empty_bar[stage]));
-    if (++stage == nstage) { stage = 0; fpar ^= 1u; }
   };
   const uint64_t c2 = pk(c, c);
   // online (max, sum) update with one item of one row: one max, one rescale, paired FMA / add
@@ -390,21 +397,20 @@ __global__ void __launch_bounds__(kStreamThreads, BF16 ? 3 : 1) stream_kernel(co
       }
     }
 
-    // ---- pass 1: online (max, sum) of both rows, item by item from the ring
+    // ---- pass 1: online (max, sum) of both rows, item by item
     float mt = ninf(), st = 0.f, md = ninf(), sd = 0.f;
     for (int it = 0; it < nitems; ++it) {
-      wait_item();
-      const uint8_t* rt_st = ring + (stage * 2) * ITEM_BYTES;
+      next_item();
       uint32_t Wt[IW];
-      read_item(Wt, rt_st, gt, it);
+      read_item(Wt, 0, gt, it);
       if (pair) {
         uint32_t Wd[IW];
-        read_item(Wd, rt_st + ITEM_BYTES, gd, it);
-        release_item();
+        read_item(Wd, 1, gd, it);
+        done_item();
         fold_item(Wt, mt, st);
         fold_item(Wd, md, sd);
       } else {
-        release_item();
+        done_item();
         fold_item(Wt, mt, st);
       }
     }
@@ -466,15 +472,38 @@ __global__ void __launch_bounds__(kStreamThreads, BF16 ? 3 : 1) stream_kernel(co
 
     // ---- pass 2: residual and p masses per (item, warp) -> CTA totals -> exchange #2
     float Rtot = 0.f, Ptot = 0.f;
+    // a pair that passes the test and draws nothing needs only alpha = sum min(p, q), and
+    // min(2^a, 2^b) = 2^min(a, b): one exp2 per logit pair, no per-item masses
+    const bool alpha_only = pair && !rejects && !pdraw;
     if (p2) {
       const uint64_t noff_t = pk(-offt, -offt), noff_d = pk(-offd, -offd), neg1 = pk(-1.f, -1.f);
+      if (alpha_only) {
+        uint64_t aacc = pk(0.f, 0.f);
+        for (int it = 0; it < nitems; ++it) {
+          next_item();
+          uint32_t Wt[IW], Wd[IW];
+          read_item(Wt, 0, gt, it);
+          read_item(Wd, 1, gd, it);
+          done_item();
+#pragma unroll
+          for (int i = 0; i < NP; ++i) {
+            float a0, a1, b0, b1;
+            upk(ffma2(pair_of<BF16>(Wt, i), c2, noff_t), a0, a1);
+            upk(ffma2(pair_of<BF16>(Wd, i), c2, noff_d), b0, b1);
+            aacc = fadd2(aacc, pk(ex2(fminf(a0, b0)), ex2(fminf(a1, b1))));
+          }
+        }
+        float a0, a1;
+        upk(aacc, a0, a1);
+        const float aw = warp_sum(a0 + a1);
+        if (lane == 0) part[par][0][warp] = make_float2(aw, 0.f);
+      } else {
       for (int it = 0; it < nitems; ++it) {
-        wait_item();
-        const uint8_t* rt_st = ring + (stage * 2) * ITEM_BYTES;
+        next_item();
         uint32_t Wt[IW], Wd[IW];
-        read_item(Wt, rt_st, gt, it);
-        if (pair) read_item(Wd, rt_st + ITEM_BYTES, gd, it);
-        release_item();
+        read_item(Wt, 0, gt, it);
+        if (pair) read_item(Wd, 1, gd, it);
+        done_item();
         uint64_t pacc = pk(0.f, 0.f), racc = pacc;
 #pragma unroll
         for (int i = 0; i < NP; ++i) {
@@ -492,24 +521,40 @@ __global__ void __launch_bounds__(kStreamThreads, BF16 ? 3 : 1) stream_kernel(co
         float p0, p1, r0, r1;
         upk(pacc, p0, p1);
         upk(racc, r0, r1);
-        const float rw = warp_sum(r0 + r1), pw = warp_sum(p0 + p1);
-        if (lane == 0) part[par][it][warp] = make_float2(rw, pw);
-      }
-      consumers_sync();                       // every warp's (item, warp) masses are in `part`
-      float rc = 0.f, pc = 0.f;               // CTA totals, summed in (item, warp) order
-      for (int it = 0; it < nitems; ++it)
+        // lanes 0-15 end with the warp's R, lanes 16-31 with its P (one exchange of each at 16)
+        const bool hi = (lane & 16) != 0;
+        float keep = hi ? p0 + p1 : r0 + r1;
+        keep += __shfl_xor_sync(0xffffffffu, hi ? r0 + r1 : p0 + p1, 16);
 #pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          const float2 v = part[par][it][w];
-          rc += v.x;
-          pc += v.y;
+        for (int o = 8; o; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
+        if ((lane & 15) == 0) reinterpret_cast<float*>(&part[par][it][warp])[lane >> 4] = keep;
+      }
+      }
+      // (item, warp) masses in `part`: alpha-only units have one item row holding sum min(p, q)
+      const int pitems = alpha_only ? 1 : nitems;
+      consumers_sync();                       // every warp's (item, warp) masses are in `part`
+      if (warp == 0) {
+        // CTA totals: lane l sums entries l*EP .. l*EP+EP-1 in (item, warp) order, then a scan
+        // across lanes -- the same grouping the owner search below uses
+        float rl = 0.f, pl = 0.f;
+#pragma unroll
+        for (int q = 0; q < EP; ++q) {
+          const int e = lane * EP + q, iti = e / NW, wi = e - iti * NW;
+          if (iti < pitems) {
+            const float2 v = part[par][iti][wi];
+            rl += v.x;
+            pl += v.y;
+          }
         }
-      if (warp == 0 && lane < static_cast<int>(C)) {
-        const uint32_t dst = smem_addr(&mbox2[par][rank]);
-        const uint32_t rdst = peer_addr(dst, lane);
-        const uint32_t rbar = peer_addr(smem_addr(&x2_bar[par]), lane);
-        st_async_f32(rdst, rc, rbar);
-        st_async_f32(rdst + 4, pc, rbar);
+        const float rc = __shfl_sync(0xffffffffu, warp_incl_scan(rl, lane), 31);
+        const float pc = __shfl_sync(0xffffffffu, warp_incl_scan(pl, lane), 31);
+        if (lane < static_cast<int>(C)) {
+          const uint32_t dst = smem_addr(&mbox2[par][rank]);
+          const uint32_t rdst = peer_addr(dst, lane);
+          const uint32_t rbar = peer_addr(smem_addr(&x2_bar[par]), lane);
+          st_async_f32(rdst, rc, rbar);
+          st_async_f32(rdst + 4, pc, rbar);
+        }
       }
       if (!xabort && !mbar_wait_cluster_bounded(smem_addr(&x2_bar[par]), (x2ph >> par) & 1u, xlimit)) {
         xabort = true;
@@ -541,7 +586,6 @@ __global__ void __launch_bounds__(kStreamThreads, BF16 ? 3 : 1) stream_kernel(co
           continue;
         }
         // (item, warp) entries of this CTA in order: lane l holds entries l*EP .. l*EP+EP-1
-        constexpr int EP = kStreamMaxItems * NW / 32;
         float mw[EP];
 #pragma unroll
         for (int q = 0; q < EP; ++q) {
@@ -620,10 +664,13 @@ __global__ void __launch_bounds__(kStreamThreads, BF16 ? 3 : 1) stream_kernel(co
       UnitRec* r = P.recs + u;
       r->px = px;
       r->qx = qx;
-      r->alpha = pair ? fminf(fmaxf(Ptot - Rtot, 0.f), 1.f) : 0.f;
-      r->R = Rtot;
+      // alpha-only units carry sum min(p, q) in the first total; R is then only informative
+      const float alpha = alpha_only ? Rtot : Ptot - Rtot;
+      r->alpha = pair ? fminf(fmaxf(alpha, 0.f), 1.f) : 0.f;
+      r->R = alpha_only ? fmaxf(1.f - Rtot, 0.f) : Rtot;
     }
   }
+  cp_async_wait<0>();        // only empty groups remain; retire them before leaving
   cluster_sync_relaxed();   // no CTA leaves while a peer may still write into its shared memory
 }
 

@@ -205,13 +205,14 @@ spec_status_t spec_verify_chain_greedy_static(const void* target_logits, const v
                                               int32_t* out_status, void* stream);
 
 /*
- * Test hook: iteration limit of every bounded on-device wait (default
- * 1 << 22 polls).  0 makes every such wait give up at once, which sets
- * SPEC_ERR_DEVICE_TIMEOUT; in-flight copies are still drained with the
- * default limit before a kernel returns.  Negative restores the default.
+ * Test hook: wall-time limit, in microseconds, of every bounded on-device
+ * wait (default 200000, i.e. 200 ms; measured with the GPU's global timer).
+ * 0 makes every such wait give up at once, which sets
+ * SPEC_ERR_DEVICE_TIMEOUT; copies already issued are still drained (up to
+ * 100 ms each) before a kernel returns.  Negative restores the default.
  * Process-wide; not for production use.
  */
-void spec_debug_set_wait_limit(long long polls);
+void spec_debug_set_wait_limit(long long limit_us);
 
 /*
  * Tuning hooks (process-wide, not for production use).  spec_debug_set_plan

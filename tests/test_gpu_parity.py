@@ -174,6 +174,40 @@ def test_greedy_planted_ties_lowest_index(sv):
     assert out.accepted.cpu()[1].item() == 1
 
 
+# ---------------------------------------------------------------- greedy kernels
+
+GREEDY_CASES = [
+    # (B, K, V, dtype)
+    (3, 2, 8, torch.bfloat16),        # one partial tile: most lanes read -inf
+    (2, 3, 1000, torch.float32),      # fp32 partial tile
+    (2, 4, 2048, torch.bfloat16),     # exactly one tile per row
+    (3, 1, 20008, torch.bfloat16),    # ragged last tile
+    (2, 5, 12300, torch.float32),     # fp32 ragged
+    (5, 3, 128000, torch.bfloat16),   # warp runs that span rows and requests
+    (1, 0, 65536, torch.bfloat16),    # K = 0
+    (2, 3, 1023, torch.bfloat16),     # unaligned rows: element-wise loads
+]
+
+
+@pytest.mark.parametrize("B,K,V,dtype", GREEDY_CASES)
+def test_greedy_fused_and_separate_cut_agree(sv, B, K, V, dtype):
+    w = W.random_case(seed=7 * B + 13 * K + V, B=B, K=K, V=V, T=0.0, dtype=dtype)
+    ref = oracle_verify(w)
+    outs = []
+    try:
+        for variant in (0, 2):   # the cut fused into the argmax kernel, then in its own kernel
+            sv.set_variant(variant)
+            out = _run_chain(sv, w, want_alpha=K > 0)
+            compare(out, ref, w)
+            outs.append(out)
+    finally:
+        sv.set_variant(0)
+    assert torch.equal(outs[1].tokens, outs[0].tokens) and torch.equal(outs[1].accepted, outs[0].accepted)
+    if K > 0:
+        assert torch.equal(outs[1].alpha, outs[0].alpha)
+    assert sv.default_workspace().status() == 0
+
+
 # ---------------------------------------------------------------- other entry points
 
 def test_overlap_alpha_matches_oracle(sv):
