@@ -253,7 +253,8 @@ def last_plan() -> dict:
 
 
 def set_variant(variant: int = 0):
-    """Test hook, greedy path: bit 1 runs the cut in its own kernel (0 = fused into the argmax kernel)."""
+    """Test hook, greedy path: bit 1 runs the cut in its own kernel (0 = fused into the argmax kernel);
+    bit 2 launches every resident CTA slot with the tiles spread evenly over the warps."""
     lib().spec_debug_set_variant(int(variant))
 
 

@@ -58,7 +58,7 @@ size_t ws_bytes_needed(int B, int K) {
 
 // Test and tuning hooks: the last row-kernel plan, and optional overrides (0 = automatic).
 std::atomic<int> g_force_nt{0}, g_force_cluster{0}, g_force_nstage{0};
-std::atomic<int> g_variant{0};   // greedy path: bit 1 separate cut kernel
+std::atomic<int> g_variant{0};   // greedy path: bit 1 separate cut kernel, bit 2 one full resident wave
 int g_last_plan[8] = {0};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -288,6 +288,7 @@ spec_status_t launch_greedy(const void* target, const void* draft, int dtype, in
   // warp is left with an extra tile after the others finish
   const long long per_warp = (p.total_tiles + 8ll * grid_cap - 1) / (8ll * grid_cap);
   long long grid = (p.total_tiles + 8 * per_warp - 1) / (8 * per_warp);
+  if (variant & 4) grid = (p.total_tiles + 7) / 8;   // every resident CTA slot, tiles spread evenly
   if (grid > grid_cap) grid = grid_cap;
   if (grid < 1) grid = 1;
   if (sv::launch_argmax(dtype == SPEC_BF16, p, static_cast<int>(grid), stream) != cudaSuccess) return SPEC_ERR_CUDA;
@@ -563,7 +564,7 @@ void spec_debug_set_plan(int threads, int cluster, int nstage) {
   g_force_nstage.store(nstage > 0 && nstage <= 16 ? nstage : 0);
 }
 
-void spec_debug_set_variant(int variant) { g_variant.store(variant & 3); }
+void spec_debug_set_variant(int variant) { g_variant.store(variant & 7); }
 
 void spec_debug_last_plan(int32_t* out8) {
   if (out8) std::memcpy(out8, g_last_plan, sizeof(g_last_plan));

@@ -223,7 +223,9 @@ void spec_debug_set_wait_limit(long long limit_us);
  * clusters, slice, stages, ring bytes, flags}.
  */
 void spec_debug_set_plan(int threads, int cluster, int nstage);
-/* Greedy-path schedule variant: bit 1 runs the cut in a separate kernel (0 = fused, default). */
+/* Greedy-path schedule variant: bit 1 runs the cut in a separate kernel (0 = fused, default);
+ * bit 2 launches every resident CTA slot, the tiles spread evenly over the warps (default: the
+ * fewest CTAs that give every warp the same number of tiles). */
 void spec_debug_set_variant(int variant);
 void spec_debug_last_plan(int32_t* out8);
 
