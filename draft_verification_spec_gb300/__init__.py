@@ -240,7 +240,8 @@ def alloc_budget(alpha, budget: int, stream=None, workspace: Optional[Workspace]
 
 
 def set_plan(threads: int = 0, cluster: int = 0, nstage: int = 0):
-    """Tuning hook: force the row kernel's CTA size, cluster size and staging depth (0 = automatic)."""
+    """Tuning hook: force the sampling row kernel's cluster size (0 = automatic); `threads` and
+    `nstage` are accepted and ignored."""
     lib().spec_debug_set_plan(int(threads), int(cluster), int(nstage))
 
 

@@ -38,8 +38,9 @@
  *   (spec_workspace_init) before its first use and again whenever the same
  *   buffer is passed with a different ws_bytes.  Calls that share a
  *   workspace must be ordered on one stream.
- * - A call launches two kernels on `stream`: the row kernel and a small
- *   kernel (the serial cut, or the budget and the cut) chained to it with
+ * - Launches on `stream`: at T == 0 without a budget one kernel (the argmax,
+ *   with the serial cut fused in); otherwise the row kernel and a small kernel
+ *   (the serial cut, or the budget and the cut) chained to it with
  *   programmatic dependent launch.
  * - Logits may contain -inf (probability 0); each row needs one finite
  *   value.  NaN / +inf give unspecified tokens (they are not scanned for).
@@ -216,11 +217,14 @@ void spec_debug_set_wait_limit(long long limit_us);
 
 /*
  * Tuning hooks (process-wide, not for production use).  spec_debug_set_plan
- * forces the row kernel's threads per CTA (256 or 512), cluster size (CTAs
- * per row, 1..16; must cover V with 32 logits per thread) and staging depth
- * (1..4); 0 keeps the automatic choice.  spec_debug_last_plan writes the last
- * launched plan: {threads, cluster, clusters launched, max co-resident
- * clusters, slice, stages, ring bytes, flags}.
+ * forces the sampling row kernel's cluster size (CTAs per row, 1..16; the
+ * cluster must cover V with 32 items of 4096 logits, else the call returns
+ * SPEC_ERR_UNSUPPORTED); 0 keeps the automatic choice.  `threads` and
+ * `nstage` are accepted for compatibility and ignored (the kernel runs 256
+ * threads per CTA and a fixed copy pipeline).  spec_debug_last_plan writes
+ * the last launched plan: sampling kernel {threads, cluster, clusters
+ * launched, max co-resident clusters, slice, stages, ring bytes, flags};
+ * argmax kernel {threads, 1, grid, resident CTAs, tile, 0, 0, -1}.
  */
 void spec_debug_set_plan(int threads, int cluster, int nstage);
 /* Greedy-path schedule variant: bit 1 runs the cut in a separate kernel (0 = fused, default);
