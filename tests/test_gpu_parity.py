@@ -326,3 +326,60 @@ def test_repeated_calls_deterministic(sv):
     o2 = sv.verify_chain(t, d, x, u, w.temperature, want_alpha=True)
     torch.cuda.synchronize()
     assert torch.equal(o1.tokens, o2.tokens) and torch.equal(o1.alpha, o2.alpha)
+
+
+# ---------------------------------------------------------------- paths not covered above
+
+def test_greedy_block_with_budget(sv):
+    # T = 0 with a budget: one-hot alpha from the argmax keys, the budget, then the cut
+    w = W.random_case(seed=21, B=6, K=5, V=9000, T=0.0, dtype=torch.bfloat16)
+    N = 13
+    out = _run_block(sv, w, budget=N)
+    a_ref = oracle_alpha(w)
+    np.testing.assert_array_equal(to_np(out.alpha), a_ref)
+    br = O.alloc_budget(a_ref, N)
+    np.testing.assert_array_equal(out.depth.cpu().numpy(), br.depth)     # dyadic keys: exact
+    compare(out, oracle_verify(w, depth=br.depth), w)
+    assert sv.default_workspace().status() == 0
+
+
+def test_greedy_chain_with_depth(sv):
+    w = W.random_case(seed=22, B=5, K=4, V=7000, T=0.0, dtype=torch.bfloat16)
+    depth = np.array([0, 1, 4, 2, 3], dtype=np.int32)
+    out = _run_chain(sv, w, want_alpha=True, depth=depth)
+    compare(out, oracle_verify(w, depth=depth), w)
+    assert np.all(out.accepted.cpu().numpy() <= depth)
+
+
+def test_overlap_alpha_fp32(sv):
+    w = W.random_case(seed=23, B=3, K=4, V=5000, T=0.7, dtype=torch.float32)
+    t, d, _, _ = _dev(w)
+    a, c, E = sv.overlap_alpha(t, d, w.temperature)
+    torch.cuda.synchronize()
+    ra, rc, rE = O.overlap_stats(w.target.double().numpy(), w.draft.double().numpy(), w.temperature)
+    np.testing.assert_allclose(to_np(a), ra, atol=1e-5, rtol=0)
+    np.testing.assert_allclose(to_np(c), rc, atol=1e-5, rtol=0)
+    np.testing.assert_allclose(to_np(E), rE, atol=1e-4, rtol=0)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_k0_sampling_is_plain_decoding(sv, dtype):
+    # K = 0 at T > 0: no draft, the emitted token is the draw from p_0
+    w = W.random_case(seed=24, B=4, K=0, V=3000, T=0.8, dtype=dtype)
+    out = _run_chain(sv, w, want_alpha=False)
+    compare(out, oracle_verify(w), w)
+    assert np.all(out.accepted.cpu().numpy() == 0)
+
+
+def test_fp32_block_with_budget(sv):
+    w = W.random_case(seed=25, B=5, K=6, V=6000, T=1.1, dtype=torch.float32)
+    N = 11
+    out = _run_block(sv, w, budget=N)
+    a_ref = oracle_alpha(w)
+    np.testing.assert_allclose(to_np(out.alpha), a_ref, atol=1e-5, rtol=0)
+    gdepth = out.depth.cpu().numpy()
+    assert gdepth.sum() == min(N, w.B * w.K)
+    br = O.alloc_budget(a_ref, N)
+    if br.margin >= 1e-5:
+        np.testing.assert_array_equal(gdepth, br.depth)
+    compare(out, oracle_verify(w, depth=gdepth), w)
