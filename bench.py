@@ -222,7 +222,7 @@ def profiled_traffic(kind: str, config_name: str):
 
 # ---------------------------------------------------------------- GPU arm
 
-class GpuRunner:
+class DeviceRunner:
     """Device-resident copies of one workload and a CUDA graph of back-to-back calls."""
 
     def __init__(self, w, name, device, min_bytes):
@@ -309,7 +309,7 @@ def run_gpu(args, rank, local_rank, world):
     min_bytes = 4 * l2 + 1
 
     w = make_workload(args.config, rank)
-    r = GpuRunner(w, args.config, dev, min_bytes)
+    r = DeviceRunner(w, args.config, dev, min_bytes)
     # warm-up (untimed)
     r.run(args.warmup, chunk=max(1, min(args.warmup, 500)))
     torch.cuda.synchronize()
@@ -354,7 +354,7 @@ def run_gpu(args, rank, local_rank, world):
         for name in args.extra:
             try:
                 wx = make_workload(name, 0)
-                rx = GpuRunner(wx, name, dev, min_bytes)
+                rx = DeviceRunner(wx, name, dev, min_bytes)
                 rx.run(5, chunk=5)
                 nsteps = args.extra_steps
                 msx = rx.run(nsteps)
