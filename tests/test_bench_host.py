@@ -1,0 +1,56 @@
+"""CPU checks of the benchmark's host logic: the reference arm's JSON line, the algorithmic byte
+count behind the roofline, and the guard that drops a profiled DRAM traffic figure once the
+kernel's sources no longer match the capture."""
+import io
+import json
+import os
+import sys
+from contextlib import redirect_stdout
+
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import workloads as W  # noqa: E402
+
+
+def test_reference_arm_prints_one_contract_line():
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.main(["--impl", "reference", "--config", "tiny_chain", "--steps", "3", "--warmup", "3"])
+    lines = [ln for ln in buf.getvalue().splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 3 and d["warmup"] == 3
+    assert d["value"] > 0 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_algorithmic_bytes_count_each_logit_once():
+    w = W.greedy_mtp(B=2, V=1000)
+    e = w.target.element_size()
+    target_only = 2 * 4 * 1000 * e
+    small = 2 * 3 * 4 + 2 * 4 * 4 + 2 * 4          # ids, emitted tokens, accepted counts
+    assert bench.algorithmic_bytes(w, False) == target_only + small
+    w2 = W.random_case(seed=1, B=2, K=3, V=1000, T=0.9, dtype=torch.bfloat16)
+    with_draft = target_only + 2 * 3 * 1000 * e
+    assert bench.algorithmic_bytes(w2, True) == with_draft + small + 2 * 4 * 4   # + uniforms
+
+
+def test_profiled_traffic_needs_matching_sources(tmp_path, monkeypatch):
+    path = tmp_path / "traffic.txt"
+    good = bench.kernel_source_hash("greedy")
+    path.write_text(f"# comment\nkernel_source_hash = {good}\ngreedy_mtp.dram_bytes_per_launch = 123456\n")
+    monkeypatch.setitem(bench.KERNELS["greedy"], "traffic", str(path))
+    assert bench.profiled_traffic("greedy", "greedy_mtp") == 123456
+    assert bench.profiled_traffic("greedy", "stochastic_mtp") is None       # no figure for that workload
+    path.write_text("kernel_source_hash = 0000000000000000\ngreedy_mtp.dram_bytes_per_launch = 123456\n")
+    assert bench.profiled_traffic("greedy", "greedy_mtp") is None           # the kernel changed since
+
