@@ -86,6 +86,12 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
 }
+// The same copy, full 16 bytes, with compile-time byte offsets on both addresses.
+template <uint32_t SO, uint32_t GO>
+__device__ __forceinline__ void cp_async16_at(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0+%2], [%1+%3], 16;" ::"r"(dst), "l"(src), "n"(SO), "n"(GO)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
@@ -215,10 +221,32 @@ __global__ void __launch_bounds__(kStreamThreads, BF16 ? 3 : 1) stream_kernel(co
     ird = static_cast<const uint8_t*>(P.draft) + ((static_cast<size_t>(b) * K + k) * static_cast<size_t>(V) + lo) * ESZ;
   };
   int istage = 0;
+  // this thread's first logit of an item and its first 16-byte slot of stage 0, row 0
+  const int tofs = warp * kStreamWarpSpan + lane * kChunk;
+  const uint32_t sbase = smem_addr(&stage_buf[warp * 32 + lane]);
+  constexpr uint32_t kRowBytes = NV * HP * 256 * 16;                // one row of one stage
+  auto issue_whole = [&](uint32_t s0, const uint8_t* src) {         // every piece of an item
+    static_assert(kStreamNV == 2, "two chunks per lane");
+    constexpr uint32_t GJ = 32 * kChunk * ESZ;                      // chunk j + 1 of a lane, in bytes
+    cp_async16_at<0u, 0u>(s0, src);
+    if constexpr (HP == 1) {
+      cp_async16_at<4096u, GJ>(s0, src);
+    } else {
+      cp_async16_at<4096u, 16u>(s0, src);
+      cp_async16_at<8192u, GJ>(s0, src);
+      cp_async16_at<12288u, GJ + 16u>(s0, src);
+    }
+  };
   auto issue_next = [&]() {
     if (tma && iu < nunits && nitems > 0) {
       const int e0 = iit * kStreamItem;
       const int nval = min(kStreamItem, n - e0);
+      if (nval == kStreamItem) {
+        const size_t g0 = static_cast<size_t>(e0 + tofs) * ESZ;
+        const uint32_t s0 = sbase + static_cast<uint32_t>(istage) * (2u * kRowBytes);
+        issue_whole(s0, irt + g0);
+        if (ipair) issue_whole(s0 + kRowBytes, ird + g0);
+      } else {
 #pragma unroll
       for (int j = 0; j < NV; ++j) {
         const int o = warp * kStreamWarpSpan + (j * 32 + lane) * kChunk;
@@ -234,6 +262,7 @@ __global__ void __launch_bounds__(kStreamThreads, BF16 ? 3 : 1) stream_kernel(co
               cp_async16(smem_addr(&stage_buf[q + NV * HP * 256]), ird + go, static_cast<uint32_t>(sb));
           }
         }
+      }
       }
       if (++iit == nitems) {
         iit = 0;
