@@ -43,8 +43,8 @@ KERNELS = {
     "greedy": {"name": "sv::argmax_kernel<bf16> (argmax + fused cut, one launch)",
                "sources": ["argmax_kernel.cuh", "spec_device.cuh", "spec_internal.h", "budget_cut.cu", "api.cu"],
                "traffic": os.path.join(ROOT, "profiles", "argmax_kernel_traffic.txt")},
-    "sampling": {"name": "sv::stream_kernel<bf16> (+ sv::cut_kernel / budget_cut_kernel, PDL-chained)",
-                 "sources": ["stream_kernel.cuh", "spec_async.cuh", "spec_device.cuh", "spec_internal.h", "row_bf16.cu", "api.cu"],
+    "sampling": {"name": "sv::sample_kernel<bf16> (+ sv::cut_kernel / budget_cut_kernel, PDL-chained)",
+                 "sources": ["sample_kernel.cuh", "spec_async.cuh", "spec_device.cuh", "spec_internal.h", "row_bf16.cu", "api.cu"],
                  "traffic": os.path.join(ROOT, "profiles", "stream_kernel_traffic.txt")},
 }
 
@@ -251,15 +251,15 @@ class DeviceRunner:
         self.kernel_kind = "greedy" if w.temperature == 0 else "sampling"
         self.graphs = {}
 
-    def step(self, i):
+    def step(self, i, tuning=None):
         t, d, x, u = self.sets[i % self.nsets]
         w, sv = self.w, self.sv
         if self.kind == "chain":
             sv.verify_chain(t, d, x, u, w.temperature, want_alpha=False, stream=self.stream,
-                            workspace=self.ws, out=self.out)
+                            workspace=self.ws, out=self.out, tuning=tuning)
         else:
             sv.verify_block(t, d, x, u, w.temperature, budget=w.budget, want_stats=True,
-                            stream=self.stream, workspace=self.ws, out=self.out)
+                            stream=self.stream, workspace=self.ws, out=self.out, tuning=tuning)
 
     def launches_per_step(self):
         # greedy without a budget: one argmax kernel with the cut fused in; otherwise the row
@@ -313,10 +313,11 @@ def run_gpu(args, rank, local_rank, world):
     # warm-up (untimed)
     r.run(args.warmup, chunk=max(1, min(args.warmup, 500)))
     torch.cuda.synchronize()
+    tuning = sv.Tuning()
     with torch.cuda.stream(r.stream):
-        r.step(0)
+        r.step(0, tuning=tuning)
     torch.cuda.synchronize()
-    plan = sv.last_plan()
+    plan = tuning.plan
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if sampler:
         sampler.start()

@@ -134,6 +134,29 @@ class VerifyOutput:
     depth: Optional[torch.Tensor] = None
 
 
+class Tuning:
+    """Per-call test and tuning knobs (spec_tuning_t); the defaults leave every choice to the library.
+
+    wait_limit_us: 0 default (200 ms), > 0 a limit, < 0 every bounded device wait gives up at once.
+    cluster: sampling kernel CTAs per row (0 automatic).  greedy_variant: bit 1 separate cut kernel,
+    bit 2 every resident CTA slot.  After the call, ``plan`` holds the launched plan.
+    """
+
+    KEYS = ("threads", "cluster", "clusters", "max_clusters", "slice", "stages", "ring_bytes", "flags")
+
+    def __init__(self, wait_limit_us: int = 0, cluster: int = 0, greedy_variant: int = 0):
+        self._plan = (ctypes.c_int32 * 8)()
+        self._c = _lib.SpecTuning(int(wait_limit_us), int(cluster), int(greedy_variant),
+                                  ctypes.cast(self._plan, ctypes.c_void_p))
+
+    @property
+    def plan(self) -> dict:
+        return dict(zip(self.KEYS, list(self._plan)))
+
+    def ref(self):
+        return ctypes.byref(self._c)
+
+
 def _validate(target, draft, tokens, uniforms, temperature, draft_needed, tokens_needed=True):
     if target.dim() != 3:
         raise ValueError("target logits must be [B, K+1, V]")
@@ -158,8 +181,9 @@ def _validate(target, draft, tokens, uniforms, temperature, draft_needed, tokens
 
 
 def verify_chain(target, draft, tokens, uniforms, temperature: float, depth=None, want_alpha=False,
-                 stream=None, workspace: Optional[Workspace] = None, out: Optional[VerifyOutput] = None):
-    """MTP-chain verification (spec_verify_chain)."""
+                 stream=None, workspace: Optional[Workspace] = None, out: Optional[VerifyOutput] = None,
+                 tuning: Optional[Tuning] = None):
+    """MTP-chain verification (spec_verify_chain; spec_verify_tuned when `tuning` is given)."""
     B, K, V, code = _validate(target, draft, tokens, uniforms, temperature,
                               draft_needed=(K_pos(target) > 0 and (temperature > 0 or want_alpha)))
     dev = target.device
@@ -171,6 +195,12 @@ def verify_chain(target, draft, tokens, uniforms, temperature: float, depth=None
                            torch.empty(B, K, dtype=torch.float32, device=dev) if want_alpha else None)
     ws = (workspace or default_workspace(stream))
     buf = ws.get(B, K, V, code, stream)
+    if tuning is not None:
+        _check(lib().spec_verify_tuned(_ptr(target), _ptr(draft), code, _ptr(tokens), _ptr(uniforms), B, K, V,
+                                       float(temperature), _ptr(depth), -1, 0, _ptr(out.tokens),
+                                       _ptr(out.accepted), _ptr(out.alpha), None, None, None, _ptr(buf),
+                                       buf.numel(), _stream_ptr(stream), tuning.ref()), "spec_verify_tuned")
+        return out
     _check(lib().spec_verify_chain(_ptr(target), _ptr(draft), code, _ptr(tokens), _ptr(uniforms), B, K, V,
                                    float(temperature), _ptr(depth), _ptr(out.tokens), _ptr(out.accepted),
                                    _ptr(out.alpha), _ptr(buf), buf.numel(), _stream_ptr(stream)),
@@ -184,7 +214,7 @@ def K_pos(target) -> int:
 
 def verify_block(target, draft, tokens, uniforms, temperature: float, depth=None, budget: Optional[int] = None,
                  want_stats=True, stream=None, workspace: Optional[Workspace] = None,
-                 out: Optional[VerifyOutput] = None):
+                 out: Optional[VerifyOutput] = None, tuning: Optional[Tuning] = None):
     """DFly-block verification (spec_verify_block): alpha, prefix confidences, expected length,
     and optionally the batch-level budget (depth chosen in the same call)."""
     need_draft = K_pos(target) > 0 and (temperature > 0 or want_stats or budget is not None)
@@ -201,6 +231,13 @@ def verify_block(target, draft, tokens, uniforms, temperature: float, depth=None
                            torch.empty(B, dtype=torch.int32, device=dev) if budget is not None else None)
     ws = (workspace or default_workspace(stream))
     buf = ws.get(B, K, V, code, stream)
+    if tuning is not None:
+        _check(lib().spec_verify_tuned(_ptr(target), _ptr(draft), code, _ptr(tokens), _ptr(uniforms), B, K, V,
+                                       float(temperature), _ptr(depth), -1 if budget is None else int(budget), 0,
+                                       _ptr(out.tokens), _ptr(out.accepted), _ptr(out.alpha), _ptr(out.cum_alpha),
+                                       _ptr(out.expected_len), _ptr(out.depth), _ptr(buf), buf.numel(),
+                                       _stream_ptr(stream), tuning.ref()), "spec_verify_tuned")
+        return out
     _check(lib().spec_verify_block(_ptr(target), _ptr(draft), code, _ptr(tokens), _ptr(uniforms), B, K, V,
                                    float(temperature), _ptr(depth), -1 if budget is None else int(budget),
                                    _ptr(out.tokens), _ptr(out.accepted), _ptr(out.alpha), _ptr(out.cum_alpha),
@@ -210,7 +247,8 @@ def verify_block(target, draft, tokens, uniforms, temperature: float, depth=None
     return out
 
 
-def overlap_alpha(target, draft, temperature: float, stream=None, workspace: Optional[Workspace] = None):
+def overlap_alpha(target, draft, temperature: float, stream=None, workspace: Optional[Workspace] = None,
+                  tuning: Optional[Tuning] = None):
     """alpha [B, K], prefix confidences [B, K], expected length [B] (spec_overlap_alpha)."""
     B, K, V, code = _validate(target, draft, None, None, temperature, draft_needed=True, tokens_needed=False)
     dev = target.device
@@ -219,6 +257,11 @@ def overlap_alpha(target, draft, temperature: float, stream=None, workspace: Opt
     E = torch.empty(B, dtype=torch.float32, device=dev)
     ws = (workspace or default_workspace(stream))
     buf = ws.get(B, K, V, code, stream)
+    if tuning is not None:
+        _check(lib().spec_verify_tuned(_ptr(target), _ptr(draft), code, None, None, B, K, V, float(temperature),
+                                       None, -1, 1, None, None, _ptr(alpha), _ptr(cum), _ptr(E), None, _ptr(buf),
+                                       buf.numel(), _stream_ptr(stream), tuning.ref()), "spec_verify_tuned")
+        return alpha, cum, E
     _check(lib().spec_overlap_alpha(_ptr(target), _ptr(draft), code, B, K, V, float(temperature), _ptr(alpha),
                                     _ptr(cum), _ptr(E), _ptr(buf), buf.numel(), _stream_ptr(stream)),
            "spec_overlap_alpha")
@@ -239,31 +282,5 @@ def alloc_budget(alpha, budget: int, stream=None, workspace: Optional[Workspace]
     return depth, conf
 
 
-def set_plan(threads: int = 0, cluster: int = 0, nstage: int = 0):
-    """Tuning hook: force the sampling row kernel's cluster size (0 = automatic); `threads` and
-    `nstage` are accepted and ignored."""
-    lib().spec_debug_set_plan(int(threads), int(cluster), int(nstage))
-
-
-def last_plan() -> dict:
-    """The last launched row-kernel plan (threads, cluster, clusters, max_clusters, slice, stages, ring, flags)."""
-    buf = (ctypes.c_int32 * 8)()
-    lib().spec_debug_last_plan(ctypes.cast(buf, ctypes.c_void_p))
-    keys = ("threads", "cluster", "clusters", "max_clusters", "slice", "stages", "ring_bytes", "flags")
-    return dict(zip(keys, list(buf)))
-
-
-def set_variant(variant: int = 0):
-    """Test hook, greedy path: bit 1 runs the cut in its own kernel (0 = fused into the argmax kernel);
-    bit 2 launches every resident CTA slot with the tiles spread evenly over the warps."""
-    lib().spec_debug_set_variant(int(variant))
-
-
-def set_wait_limit(limit_us: int):
-    """Test hook: wall-time limit in microseconds of the kernels' bounded waits (0 = give up at
-    once, -1 restores the default of 200 ms)."""
-    lib().spec_debug_set_wait_limit(int(limit_us))
-
-
 __all__ = ["verify_chain", "verify_block", "overlap_alpha", "alloc_budget", "Workspace", "VerifyOutput",
-           "SpecError", "set_wait_limit", "set_plan", "set_variant", "last_plan", "lib"]
+           "Tuning", "SpecError", "lib"]

@@ -14,6 +14,12 @@ LIB_PATH = os.path.join(HERE, "libspecverify.so")
 c_int, c_float, c_size_t, c_void_p = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
 c_longlong = ctypes.c_longlong
 
+
+class SpecTuning(ctypes.Structure):
+    """spec_tuning_t: per-call test and tuning knobs (all zero = defaults)."""
+    _fields_ = [("wait_limit_us", c_longlong), ("cluster", c_int), ("greedy_variant", c_int),
+                ("plan_out", c_void_p)]
+
 # name -> (restype, argtypes), mirroring include/spec_verify.h
 SIGNATURES = {
     "spec_version": (c_int, []),
@@ -33,10 +39,9 @@ SIGNATURES = {
                                   c_void_p]),
     "spec_verify_chain_greedy_static": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int, c_int,
                                                 c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
-    "spec_debug_set_wait_limit": (None, [c_longlong]),
-    "spec_debug_set_plan": (None, [c_int, c_int, c_int]),
-    "spec_debug_last_plan": (None, [c_void_p]),
-    "spec_debug_set_variant": (None, [c_int]),
+    "spec_verify_tuned": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int, c_int, c_int,
+                                  c_float, c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
+                                  c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]),
 }
 
 _lib = None

@@ -1,18 +1,22 @@
-// C ABI of the verification library: argument checks, launch configuration, launches.
+// C ABI of the verification library: argument checks, launch planning, launches.
 // The declarations and their contracts are in include/spec_verify.h.
-#include <atomic>
+//
+// The library keeps no mutable state between calls except two per-device caches (kernel
+// attributes set, occupancy answers), guarded by a mutex.  Tuning and test knobs travel with
+// the call (spec_tuning_t), never through process-wide settings.
 #include <cmath>
 #include <cstring>
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <vector>
 
 #include "../../include/spec_verify.h"
 #include "spec_internal.h"
 
 namespace sv {
-const void* sample_kernel_bf16(int nt);
-const void* sample_kernel_f32(int nt);
+const void* sample_kernel_bf16();
+const void* sample_kernel_f32();
 }  // namespace sv
 
 namespace {
@@ -21,13 +25,13 @@ using sv::BudgetParams;
 using sv::RowParams;
 using sv::UnitRec;
 
-constexpr long long kDefaultWaitLimit = 200000000ll;   // ns of wall time per bounded on-device wait
-std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
-
+constexpr long long kDefaultWaitNs = 200000000ll;   // wall time per bounded on-device wait
 constexpr size_t kAlign = 256;
 constexpr int kMaxV = 262144;
 constexpr int kBudgetMaxKeys = 8192;
-constexpr size_t kRingBudgetLarge = 200 * 1024;   // per CTA when one CTA fills an SM
+constexpr int kSampThreads = 256;
+constexpr int kItemBytes = sv::kSampItemBytes;       // bytes of one row per item of the sampling kernel
+constexpr int kMaxItems = sv::kSampMaxItems;         // items per slice
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -56,24 +60,64 @@ size_t ws_bytes_needed(int B, int K) {
   return 4 * kAlign + rows * kRowBytes;
 }
 
-// Test and tuning hooks: the last row-kernel plan, and optional overrides (0 = automatic).
-std::atomic<int> g_force_nt{0}, g_force_cluster{0}, g_force_nstage{0};
-std::atomic<int> g_variant{0};   // greedy path: bit 1 separate cut kernel, bit 2 one full resident wave
-int g_last_plan[8] = {0};
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// One-time per (device, kernel) attribute setup and a cache of the cluster occupancy.
+// The knobs of one call: defaults, or the caller's spec_tuning_t.
+struct Knobs {
+  long long wait_ns = kDefaultWaitNs;
+  int cluster = 0;
+  int variant = 0;
+  int32_t* plan_out = nullptr;
+};
+Knobs knobs_of(const spec_tuning_t* t) {
+  Knobs k;
+  if (!t) return k;
+  if (t->wait_limit_us > 0) k.wait_ns = t->wait_limit_us * 1000;
+  if (t->wait_limit_us < 0) k.wait_ns = 0;
+  k.cluster = t->cluster;
+  k.variant = t->greedy_variant & 7;
+  k.plan_out = t->plan_out;
+  return k;
+}
+void report_plan(const Knobs& kn, const int (&rec)[8]) {
+  if (kn.plan_out) std::memcpy(kn.plan_out, rec, sizeof(rec));
+}
+
+// Per-device caches: kernel attributes set once, and occupancy answers.
 std::mutex g_mu;
 std::map<std::tuple<int, const void*>, bool> g_attr_done;
-std::map<std::tuple<int, const void*, int, size_t>, int> g_occ;
+std::map<std::tuple<int, const void*, int>, int> g_maxc;
+std::map<int, std::tuple<int, int, size_t>> g_dev;   // SMs, L2 bytes
+// chosen sampling plan (cluster size, clusters launched, resident clusters) per call shape
+std::map<std::tuple<int, const void*, int, int, int, int, int>, std::tuple<int, int, int>> g_plans;
+
+cudaError_t device_info(int dev, int* sms, size_t* l2) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_dev.find(dev);
+    if (it != g_dev.end()) {
+      *sms = std::get<0>(it->second);
+      *l2 = std::get<2>(it->second);
+      return cudaSuccess;
+    }
+  }
+  int s = 0, l = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&s, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&l, cudaDevAttrL2CacheSize, dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_dev[dev] = std::make_tuple(s, 0, static_cast<size_t>(l));
+  *sms = s;
+  *l2 = static_cast<size_t>(l);
+  return cudaSuccess;
+}
 
 cudaError_t prepare_kernel(int dev, const void* fn) {
   std::lock_guard<std::mutex> lk(g_mu);
   auto key = std::make_tuple(dev, fn);
   if (g_attr_done.count(key)) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kRingBudgetLarge + 4096));
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, sv::kSampRingBytes);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
@@ -81,15 +125,18 @@ cudaError_t prepare_kernel(int dev, const void* fn) {
   return cudaSuccess;
 }
 
-cudaError_t max_clusters(int dev, const void* fn, int nt, int cluster, size_t smem, int* out) {
+// Largest number of clusters of `cluster` sampling CTAs that can be resident at once.
+cudaError_t max_clusters(int dev, const void* fn, int cluster, int* out) {
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    auto it = g_occ.find(std::make_tuple(dev, fn, cluster, smem));
-    if (it != g_occ.end()) {
+    auto it = g_maxc.find(std::make_tuple(dev, fn, cluster));
+    if (it != g_maxc.end()) {
       *out = it->second;
       return cudaSuccess;
     }
   }
+  cudaError_t e = prepare_kernel(dev, fn);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -97,100 +144,108 @@ cudaError_t max_clusters(int dev, const void* fn, int nt, int cluster, size_t sm
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(cluster, 1, 1);
-  cfg.blockDim = dim3(nt, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.blockDim = dim3(kSampThreads, 1, 1);
+  cfg.dynamicSmemBytes = sv::kSampRingBytes;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  cudaError_t e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lk(g_mu);
-  g_occ[std::make_tuple(dev, fn, cluster, smem)] = n;
+  g_maxc[std::make_tuple(dev, fn, cluster)] = n;
   *out = n;
   return cudaSuccess;
 }
 
 struct RowPlan {
   const void* fn;
-  int nt, cluster, nclusters;
-  size_t smem;
+  int cluster, nclusters, maxc;
   RowParams p;
 };
 
-// Chooses threads per CTA, cluster size, slice and staging depth for a (dtype, V) pair.
-// Resident CTAs of the row kernel on this device (SMs x CTAs per SM), cached per kernel and size.
-std::map<std::tuple<int, const void*, size_t>, int> g_resident;
-cudaError_t resident_ctas(const void* fn, int nt, size_t smem, int* out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    auto it = g_resident.find(std::make_tuple(dev, fn, smem));
-    if (it != g_resident.end()) {
-      *out = it->second;
-      return cudaSuccess;
-    }
+// Estimated duration (arbitrary units) of the sampling kernel with clusters of C CTAs: the units
+// go round-robin to the clusters (pairs first), every unit streams its rows twice (HBM, then L2)
+// and pays a fixed cost for its two cluster exchanges and draws.
+double plan_cost(int C, int ncl, int npairs, int nsingle, double row_bytes, int resident_slots) {
+  const int units = npairs + nsingle;
+  if (ncl < 1) return 1e300;
+  // per-CTA bandwidth: the HBM shared by the active CTAs, capped by what one CTA's copy ring sustains
+  const double active = static_cast<double>(ncl) * C;
+  const double bw = std::fmin(6.5e12 / std::fmin(active, resident_slots), 3.0e10);
+  const double t_row = 1.5 * row_bytes / C / bw;        // two passes, the second from L2
+  const double t_unit = 2.0e-6;                         // exchanges, draws
+  double worst = 0.0;
+  for (int j = 0; j < ncl && j < units; ++j) {
+    double t = 0.0;
+    for (int u = j; u < units; u += ncl) t += (u < npairs ? 2.0 : 1.0) * t_row + t_unit;
+    worst = std::fmax(worst, t);
   }
-  e = prepare_kernel(dev, fn);
-  if (e != cudaSuccess) return e;
-  int sms = 0, per_sm = 0;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, nt, smem);
-  if (e != cudaSuccess) return e;
-  std::lock_guard<std::mutex> lk(g_mu);
-  g_resident[std::make_tuple(dev, fn, smem)] = sms * per_sm;
-  *out = sms * per_sm;
-  return cudaSuccess;
+  return worst;
 }
 
-spec_status_t plan_rows(const void* target, const void* draft, int dtype, int B, int K, int V,
-                        float T, bool need_draft, bool stats_only, RowPlan* plan) {
+spec_status_t plan_rows(const void* target, const void* draft, int dtype, int B, int K, int V, float T,
+                        bool need_draft, bool stats_only, const Knobs& kn, RowPlan* plan) {
   const bool bf16 = dtype == SPEC_BF16;
-  const bool greedy = T == 0.f;
   const int esz = bf16 ? 2 : 4;
-  // clusters of C CTAs, each CTA streaming a slice of V / C logits per row in 4096-logit items
-  const int nt = 256;                       // 8 warps, each thread streaming its own chunks
-  const int item = 4096;
-  const void* fn = bf16 ? sv::sample_kernel_bf16(nt) : sv::sample_kernel_f32(nt);
-  const int units = B * (stats_only ? K : K + 1);
-  int cluster = 0;
-  if (g_force_cluster.load()) {
-    if (g_force_cluster.load() * 32 * item < V) return SPEC_ERR_UNSUPPORTED;
-    cluster = g_force_cluster.load();
-  } else {
-    // The kernel is issue-bound and a unit's CTAs work in lockstep.  Split rows across more CTAs
-    // while each slice keeps at least 7 items (so per-unit exchanges stay small against the
-    // streaming) and there are at most 2.5 CTA-tasks (units x C) per resident CTA slot (beyond
-    // that the extra per-unit rounds cost more than the finer balance gains).  A slice holds at
-    // most 32 items.
-    int slots = 0;
-    if (resident_ctas(fn, nt, 2 * static_cast<size_t>(item) * esz * sv::kStreamStagesHost, &slots) != cudaSuccess)
-      return SPEC_ERR_CUDA;
-    const int cmin = (V + 32 * item - 1) / (32 * item);
-    cluster = 1;
-    while (cluster * 2 <= sv::kMaxCluster && static_cast<long long>(V) >= 2ll * cluster * 7 * item &&
-           static_cast<long long>(units) * cluster * 2 * 2 <= 5ll * slots)
-      cluster *= 2;
-    while (cluster < cmin) cluster *= 2;
+  const void* fn = bf16 ? sv::sample_kernel_bf16() : sv::sample_kernel_f32();
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
+  int sms = 0;
+  size_t l2 = 0;
+  if (device_info(dev, &sms, &l2) != cudaSuccess) return SPEC_ERR_CUDA;
+  const int npairs = need_draft ? B * K : 0;
+  const int nsingle = stats_only ? 0 : (need_draft ? B : B * (K + 1));
+  const int units = npairs + nsingle;
+  const double row_bytes = static_cast<double>(V) * esz;
+  // a slice holds at most kMaxItems items of 8 KB per row
+  const long long min_c = (static_cast<long long>(V) * esz + static_cast<long long>(kMaxItems) * kItemBytes - 1) /
+                          (static_cast<long long>(kMaxItems) * kItemBytes);
+  int best_c = 0, best_ncl = 0, best_maxc = 0;
+  const auto key = std::make_tuple(dev, fn, B, K, V, static_cast<int>(need_draft) | (stats_only ? 2 : 0), kn.cluster);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_plans.find(key);
+    if (it != g_plans.end()) std::tie(best_c, best_ncl, best_maxc) = it->second;
   }
-  if (cluster > sv::kMaxCluster) return SPEC_ERR_UNSUPPORTED;
-  int slice = (V + cluster - 1) / cluster;
+  if (best_c == 0) {
+    // the bytes streamed between a logit's first and second read must fit in about half the L2,
+    // or the second pass goes back to HBM; among the sizes that keep it there, the cheapest
+    // estimated schedule wins (the largest size if none does)
+    bool best_fits = false;
+    double best = 1e300;
+    for (int C = 1; C <= sv::kMaxCluster; C *= 2) {
+      if (C < min_c) continue;
+      if (kn.cluster && C != kn.cluster) continue;
+      int maxc = 0;
+      if (max_clusters(dev, fn, C, &maxc) != cudaSuccess) return SPEC_ERR_CUDA;
+      if (maxc < 1) continue;
+      const int ncl = units < maxc ? units : maxc;
+      const double window = static_cast<double>(ncl) * (need_draft ? 2.0 : 1.0) * row_bytes;
+      const bool fits = kn.cluster != 0 || window <= 0.5 * static_cast<double>(l2);
+      const double cost = plan_cost(C, ncl, npairs, nsingle, row_bytes, maxc * C);
+      const bool better = (fits && !best_fits) || (fits == best_fits && (fits ? cost < best * 0.97 : C > best_c));
+      if (best_c == 0 || better) {
+        best = cost;
+        best_fits = fits;
+        best_c = C;
+        best_ncl = ncl;
+        best_maxc = maxc;
+      }
+    }
+    if (best_c == 0) return SPEC_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_plans[key] = std::make_tuple(best_c, best_ncl, best_maxc);
+  }
+  if (best_c == 0) return SPEC_ERR_UNSUPPORTED;
+  int slice = (V + best_c - 1) / best_c;
   slice = static_cast<int>(align_up(slice, sv::kChunk));
-  if (slice > 32 * item) return SPEC_ERR_UNSUPPORTED;
-  const bool tma = (static_cast<size_t>(V) * esz) % 16 == 0 && aligned16(target) &&
-                   (!need_draft || aligned16(draft));
-  const int stage_row_bytes = item * esz;
-  const size_t stage_bytes = 2 * static_cast<size_t>(stage_row_bytes);
-  // the kernel's copy pipeline is kStreamStages items deep: bf16 64 KB per CTA (three CTAs per
-  // SM), fp32 128 KB (one CTA per SM)
-  const int nstage = sv::kStreamStagesHost;
-  (void)greedy;
+  if (static_cast<long long>(slice) * esz > static_cast<long long>(kMaxItems) * kItemBytes) return SPEC_ERR_UNSUPPORTED;
+  const bool aligned = (static_cast<size_t>(V) * esz) % 16 == 0 && aligned16(target) &&
+                       (!need_draft || aligned16(draft));
   plan->fn = fn;
-  plan->nt = nt;
-  plan->cluster = cluster;
-  plan->smem = static_cast<size_t>(nstage) * stage_bytes;
+  plan->cluster = best_c;
+  plan->nclusters = best_ncl;
+  plan->maxc = best_maxc;
   RowParams& p = plan->p;
   std::memset(&p, 0, sizeof(p));
   p.target = target;
@@ -199,54 +254,50 @@ spec_status_t plan_rows(const void* target, const void* draft, int dtype, int B,
   p.K = K;
   p.V = V;
   p.U = stats_only ? K : K + 1;
-  p.total_units = B * p.U;
+  p.total_units = units;
   p.slice = slice;
-  p.nstage = nstage;
-  p.stage_row_bytes = stage_row_bytes;
   p.flags = (need_draft ? sv::F_NEED_DRAFT : 0) | (stats_only ? sv::F_STATS_ONLY : 0) |
-            (tma ? sv::F_TMA : 0);
-  p.c = greedy ? 0.f : static_cast<float>(1.4426950408889634 / static_cast<double>(T));
-  p.wait_limit = g_wait_limit.load();
+            (aligned ? sv::F_ALIGNED : 0);
+  p.c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
+  p.wait_limit = kn.wait_ns;
   return SPEC_OK;
 }
 
-spec_status_t launch_plan(RowPlan* plan, cudaStream_t stream) {
+spec_status_t launch_plan(RowPlan* plan, const Knobs& kn, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
   if (prepare_kernel(dev, plan->fn) != cudaSuccess) return SPEC_ERR_CUDA;
-  int maxc = 0;
-  if (max_clusters(dev, plan->fn, plan->nt, plan->cluster, plan->smem, &maxc) != cudaSuccess)
-    return SPEC_ERR_CUDA;
-  if (maxc < 1) return SPEC_ERR_UNSUPPORTED;
-  const int ncl = plan->p.total_units < maxc ? plan->p.total_units : maxc;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = plan->cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(ncl * plan->cluster, 1, 1);
-  cfg.blockDim = dim3(plan->nt, 1, 1);
-  cfg.dynamicSmemBytes = plan->smem;
+  // programmatic dependent launch: the grid's prologue overlaps the preceding kernel's tail; it
+  // waits (griddepcontrol.wait) for that kernel before touching memory
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(plan->nclusters * plan->cluster, 1, 1);
+  cfg.blockDim = dim3(kSampThreads, 1, 1);
+  cfg.dynamicSmemBytes = sv::kSampRingBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   void* args[] = {&plan->p};
   if (cudaLaunchKernelExC(&cfg, plan->fn, args) != cudaSuccess) return SPEC_ERR_CUDA;
-  const int rec[8] = {plan->nt, plan->cluster, ncl, maxc, plan->p.slice, plan->p.nstage,
-                      static_cast<int>(plan->smem), plan->p.flags};
-  std::memcpy(g_last_plan, rec, sizeof(rec));
+  const int rec[8] = {kSampThreads, plan->cluster, plan->nclusters, plan->maxc, plan->p.slice,
+                      sv::kSampStages, sv::kSampRingBytes, plan->p.flags};
+  report_plan(kn, rec);
   return SPEC_OK;
 }
 
 bool bad_T(float T) { return !(T >= 0.f) || std::isinf(T); }
 
 // Greedy path: the streaming argmax kernel over target rows (and draft rows when need_draft).
-// Ring: stages of 8 tiles (16 KB bf16 / 32 KB fp32); about 64 KB per CTA.
 std::map<int, int> g_argmax_grid;
 spec_status_t launch_greedy(const void* target, const void* draft, int dtype, int B, int K, int V,
                             bool need_draft, bool stats_only, bool fused_cut, uint64_t* keys,
-                            sv::ArgmaxParams cut, cudaStream_t stream) {
+                            sv::ArgmaxParams cut, const Knobs& kn, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
   int grid_cap;
@@ -258,8 +309,7 @@ spec_status_t launch_greedy(const void* target, const void* draft, int dtype, in
       int sms = 0, per_sm = 0;
       if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SPEC_ERR_CUDA;
       // one wave of resident CTAs (the bf16 and fp32 instances differ only in registers)
-      if (sv::argmax_blocks_per_sm(dtype == SPEC_BF16, 0, &per_sm) != cudaSuccess)
-        return SPEC_ERR_CUDA;
+      if (sv::argmax_blocks_per_sm(dtype == SPEC_BF16, &per_sm) != cudaSuccess) return SPEC_ERR_CUDA;
       g_argmax_grid[gkey] = sms * (per_sm > 0 ? per_sm : 1);
       it = g_argmax_grid.find(gkey);
     }
@@ -278,23 +328,21 @@ spec_status_t launch_greedy(const void* target, const void* draft, int dtype, in
   p.tpr = (V + tile - 1) / tile;
   p.total_tiles = static_cast<long long>(B) * (p.rows_t + p.drows) * p.tpr;
   if (p.total_tiles >= (1ll << 31)) return SPEC_ERR_UNSUPPORTED;
-  const int variant = g_variant.load();
-  p.fused_cut = fused_cut && !(variant & 2);
+  p.fused_cut = fused_cut && !(kn.variant & 2);
   p.stats_only = stats_only;
-  p.wait_limit = g_wait_limit.load();
+  p.wait_limit = kn.wait_ns;
   const int esz = dtype == SPEC_BF16 ? 2 : 4;
   p.aligned = (static_cast<size_t>(V) * esz) % 16 == 0 && aligned16(target) && (!need_draft || aligned16(draft));
   // every warp takes the same number of tiles (the fewest one resident wave allows), so no
   // warp is left with an extra tile after the others finish
   const long long per_warp = (p.total_tiles + 8ll * grid_cap - 1) / (8ll * grid_cap);
   long long grid = (p.total_tiles + 8 * per_warp - 1) / (8 * per_warp);
-  if (variant & 4) grid = (p.total_tiles + 7) / 8;   // every resident CTA slot, tiles spread evenly
+  if (kn.variant & 4) grid = (p.total_tiles + 7) / 8;   // every resident CTA slot, tiles spread evenly
   if (grid > grid_cap) grid = grid_cap;
   if (grid < 1) grid = 1;
   if (sv::launch_argmax(dtype == SPEC_BF16, p, static_cast<int>(grid), stream) != cudaSuccess) return SPEC_ERR_CUDA;
-  const int rec[8] = {256, 1, static_cast<int>(grid), grid_cap, tile, 0,
-                      0, -1};
-  std::memcpy(g_last_plan, rec, sizeof(rec));
+  const int rec[8] = {256, 1, static_cast<int>(grid), grid_cap, tile, 0, 0, -1};
+  report_plan(kn, rec);
   return SPEC_OK;
 }
 
@@ -326,7 +374,7 @@ struct VerifyArgs {
   cudaStream_t stream;
 };
 
-spec_status_t run_verify(const VerifyArgs& a) {
+spec_status_t run_verify(const VerifyArgs& a, const Knobs& kn) {
   if (a.dtype != SPEC_F32 && a.dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
   if (a.B < 0 || a.K < 0 || a.V < 1 || bad_T(a.T)) return SPEC_ERR_INVALID_ARG;
   if (a.K > sv::kMaxK || a.V > kMaxV) return SPEC_ERR_UNSUPPORTED;
@@ -362,13 +410,13 @@ spec_status_t run_verify(const VerifyArgs& a) {
     cut.out_alpha = a.out_alpha;
     cut.out_cum = a.out_cum;
     cut.out_E = a.out_E;
-    st = launch_greedy(a.target, a.draft, a.dtype, a.B, a.K, a.V, need_draft, false, !budget, keys, cut,
+    st = launch_greedy(a.target, a.draft, a.dtype, a.B, a.K, a.V, need_draft, false, !budget, keys, cut, kn,
                        a.stream);
     if (st != SPEC_OK) return st;
-    if (!budget && (g_variant.load() & 2) == 0) return SPEC_OK;   // the cut ran inside the argmax kernel
+    if (!budget && (kn.variant & 2) == 0) return SPEC_OK;   // the cut ran inside the argmax kernel
   } else {
     RowPlan plan;
-    st = plan_rows(a.target, a.draft, a.dtype, a.B, a.K, a.V, a.T, need_draft, false, &plan);
+    st = plan_rows(a.target, a.draft, a.dtype, a.B, a.K, a.V, a.T, need_draft, false, kn, &plan);
     if (st != SPEC_OK) return st;
     RowParams& p = plan.p;
     p.tokens = a.tokens;
@@ -377,7 +425,7 @@ spec_status_t run_verify(const VerifyArgs& a) {
     p.recs = recs;
     p.status = status;
     if (budget) p.flags |= sv::F_ALL_PDRAWS;
-    st = launch_plan(&plan, a.stream);
+    st = launch_plan(&plan, kn, a.stream);
     if (st != SPEC_OK) return st;
   }
 
@@ -408,11 +456,64 @@ spec_status_t run_verify(const VerifyArgs& a) {
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
+spec_status_t run_overlap(const void* target_logits, const void* draft_logits, int dtype, int B, int K, int V,
+                          float temperature, float* out_alpha, float* out_cum_alpha, float* out_expected_len,
+                          void* workspace, size_t ws_bytes, cudaStream_t stream, const Knobs& kn) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+  if (B < 0 || K < 0 || V < 1 || bad_T(temperature)) return SPEC_ERR_INVALID_ARG;
+  if (K > sv::kMaxK || V > kMaxV) return SPEC_ERR_UNSUPPORTED;
+  if (B == 0 || K == 0) return SPEC_OK;
+  if (!target_logits || !draft_logits || !out_alpha) return SPEC_ERR_INVALID_ARG;
+  spec_status_t st = check_ws(workspace, ws_bytes, B, K);
+  if (st != SPEC_OK) return st;
+  const WsLayout L = ws_layout_for(ws_bytes);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  UnitRec* recs = reinterpret_cast<UnitRec*>(ws + L.recs);
+  uint64_t* keys = reinterpret_cast<uint64_t*>(ws + L.keys);
+  int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
+  const bool greedy = temperature == 0.f;
+  if (greedy) {
+    sv::ArgmaxParams cut;
+    std::memset(&cut, 0, sizeof(cut));
+    cut.counters = reinterpret_cast<int32_t*>(ws + L.counters);
+    cut.status = status;
+    cut.out_alpha = out_alpha;
+    cut.out_cum = out_cum_alpha;
+    cut.out_E = out_expected_len;
+    st = launch_greedy(target_logits, draft_logits, dtype, B, K, V, true, true, true, keys, cut, kn, stream);
+    if (st != SPEC_OK || (kn.variant & 2) == 0) return st;
+  } else {
+    RowPlan plan;
+    st = plan_rows(target_logits, draft_logits, dtype, B, K, V, temperature, true, true, kn, &plan);
+    if (st != SPEC_OK) return st;
+    plan.p.recs = recs;
+    plan.p.status = status;
+    st = launch_plan(&plan, kn, stream);
+  }
+  if (st != SPEC_OK) return st;
+  BudgetParams bp;
+  std::memset(&bp, 0, sizeof(bp));
+  bp.recs = recs;
+  bp.keys = keys;
+  bp.draft_keys = greedy;
+  bp.U = K;
+  bp.B = B;
+  bp.K = K;
+  bp.V = V;
+  bp.greedy = greedy;
+  bp.stats_only = 1;
+  bp.out_alpha = out_alpha;
+  bp.out_cum = out_cum_alpha;
+  bp.out_E = out_expected_len;
+  bp.status = status;
+  return sv::launch_cut(bp, nullptr, stream) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
 
-int spec_version(void) { return 100; }
+int spec_version(void) { return 200; }
 
 const char* spec_error_string(int status) {
   switch (status) {
@@ -462,7 +563,7 @@ spec_status_t spec_verify_chain(const void* target_logits, const void* draft_log
   VerifyArgs a = {target_logits, draft_logits, dtype, tokens, uniforms, B, K, V, temperature,
                   depth, -1, out_tokens, out_accepted, out_alpha, nullptr, nullptr, nullptr,
                   workspace, ws_bytes, static_cast<cudaStream_t>(stream)};
-  return run_verify(a);
+  return run_verify(a, Knobs());
 }
 
 spec_status_t spec_verify_block(const void* target_logits, const void* draft_logits, int dtype,
@@ -474,62 +575,35 @@ spec_status_t spec_verify_block(const void* target_logits, const void* draft_log
   VerifyArgs a = {target_logits, draft_logits, dtype, tokens, uniforms, B, K, V, temperature,
                   depth, budget_N, out_tokens, out_accepted, out_alpha, out_cum_alpha,
                   out_expected_len, out_depth, workspace, ws_bytes, static_cast<cudaStream_t>(stream)};
-  return run_verify(a);
+  return run_verify(a, Knobs());
 }
 
 spec_status_t spec_overlap_alpha(const void* target_logits, const void* draft_logits, int dtype,
                                  int B, int K, int V, float temperature, float* out_alpha,
                                  float* out_cum_alpha, float* out_expected_len, void* workspace,
                                  size_t ws_bytes, void* stream) {
-  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
-  if (B < 0 || K < 0 || V < 1 || bad_T(temperature)) return SPEC_ERR_INVALID_ARG;
-  if (K > sv::kMaxK || V > kMaxV) return SPEC_ERR_UNSUPPORTED;
-  if (B == 0 || K == 0) return SPEC_OK;
-  if (!target_logits || !draft_logits || !out_alpha) return SPEC_ERR_INVALID_ARG;
-  spec_status_t st = check_ws(workspace, ws_bytes, B, K);
-  if (st != SPEC_OK) return st;
-  const WsLayout L = ws_layout_for(ws_bytes);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  UnitRec* recs = reinterpret_cast<UnitRec*>(ws + L.recs);
-  uint64_t* keys = reinterpret_cast<uint64_t*>(ws + L.keys);
-  int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
-  const bool greedy = temperature == 0.f;
-  if (greedy) {
-    sv::ArgmaxParams cut;
-    std::memset(&cut, 0, sizeof(cut));
-    cut.counters = reinterpret_cast<int32_t*>(ws + L.counters);
-    cut.status = status;
-    cut.out_alpha = out_alpha;
-    cut.out_cum = out_cum_alpha;
-    cut.out_E = out_expected_len;
-    st = launch_greedy(target_logits, draft_logits, dtype, B, K, V, true, true, true, keys, cut,
-                       static_cast<cudaStream_t>(stream));
-    if (st != SPEC_OK || (g_variant.load() & 2) == 0) return st;
-  } else {
-    RowPlan plan;
-    st = plan_rows(target_logits, draft_logits, dtype, B, K, V, temperature, true, true, &plan);
-    if (st != SPEC_OK) return st;
-    plan.p.recs = recs;
-    plan.p.status = status;
-    st = launch_plan(&plan, static_cast<cudaStream_t>(stream));
+  return run_overlap(target_logits, draft_logits, dtype, B, K, V, temperature, out_alpha, out_cum_alpha,
+                     out_expected_len, workspace, ws_bytes, static_cast<cudaStream_t>(stream), Knobs());
+}
+
+spec_status_t spec_verify_tuned(const void* target_logits, const void* draft_logits, int dtype,
+                                const int32_t* tokens, const float* uniforms, int B, int K, int V,
+                                float temperature, const int32_t* depth, int budget_N, int stats_only,
+                                int32_t* out_tokens, int32_t* out_accepted, float* out_alpha,
+                                float* out_cum_alpha, float* out_expected_len, int32_t* out_depth,
+                                void* workspace, size_t ws_bytes, void* stream, const spec_tuning_t* tuning) {
+  const Knobs kn = knobs_of(tuning);
+  if (tuning && tuning->cluster != 0) {
+    const int c = tuning->cluster;
+    if (c < 1 || c > sv::kMaxCluster || (c & (c - 1)) != 0) return SPEC_ERR_INVALID_ARG;
   }
-  if (st != SPEC_OK) return st;
-  BudgetParams bp;
-  std::memset(&bp, 0, sizeof(bp));
-  bp.recs = recs;
-  bp.keys = keys;
-  bp.draft_keys = greedy;
-  bp.U = K;
-  bp.B = B;
-  bp.K = K;
-  bp.V = V;
-  bp.greedy = greedy;
-  bp.stats_only = 1;
-  bp.out_alpha = out_alpha;
-  bp.out_cum = out_cum_alpha;
-  bp.out_E = out_expected_len;
-  bp.status = status;
-  return sv::launch_cut(bp, nullptr, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  if (stats_only)
+    return run_overlap(target_logits, draft_logits, dtype, B, K, V, temperature, out_alpha, out_cum_alpha,
+                       out_expected_len, workspace, ws_bytes, static_cast<cudaStream_t>(stream), kn);
+  VerifyArgs a = {target_logits, draft_logits, dtype, tokens, uniforms, B, K, V, temperature,
+                  depth, budget_N, out_tokens, out_accepted, out_alpha, out_cum_alpha,
+                  out_expected_len, out_depth, workspace, ws_bytes, static_cast<cudaStream_t>(stream)};
+  return run_verify(a, kn);
 }
 
 spec_status_t spec_alloc_budget(const float* alpha, int B, int K, int budget_N, int32_t* out_depth,
@@ -552,22 +626,6 @@ spec_status_t spec_alloc_budget(const float* alpha, int B, int K, int budget_N, 
   bp.status = static_cast<int32_t*>(workspace);
   return sv::launch_budget_cut(bp, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SPEC_OK
                                                                                       : SPEC_ERR_CUDA;
-}
-
-void spec_debug_set_wait_limit(long long limit_us) {
-  g_wait_limit.store(limit_us < 0 ? kDefaultWaitLimit : limit_us * 1000);
-}
-
-void spec_debug_set_plan(int threads, int cluster, int nstage) {
-  g_force_nt.store(threads == 256 || threads == 512 ? threads : 0);
-  g_force_cluster.store(cluster > 0 && cluster <= sv::kMaxCluster ? cluster : 0);
-  g_force_nstage.store(nstage > 0 && nstage <= 16 ? nstage : 0);
-}
-
-void spec_debug_set_variant(int variant) { g_variant.store(variant & 7); }
-
-void spec_debug_last_plan(int32_t* out8) {
-  if (out8) std::memcpy(out8, g_last_plan, sizeof(g_last_plan));
 }
 
 }  // extern "C"

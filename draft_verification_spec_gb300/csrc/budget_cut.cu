@@ -134,10 +134,9 @@ cudaError_t launch_cut(const BudgetParams& p, const int32_t* depth, cudaStream_t
   return launch_pdl(reinterpret_cast<const void*>(&cut_kernel), grid, kCutThreads, 0, stream, args);
 }
 
-cudaError_t argmax_blocks_per_sm(bool bf16, int nstage, int* out) {
+cudaError_t argmax_blocks_per_sm(bool bf16, int* out) {
   const void* fn = bf16 ? reinterpret_cast<const void*>(&argmax_kernel<true>)
                         : reinterpret_cast<const void*>(&argmax_kernel<false>);
-  (void)nstage;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, fn, 256, 0);
 }
 

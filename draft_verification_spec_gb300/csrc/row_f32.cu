@@ -1,11 +1,8 @@
-// f32 instantiation of the sampling row kernel.
-#include "stream_kernel.cuh"
+// fp32 instantiation of the sampling row kernel.
+#include "sample_kernel.cuh"
 
 namespace sv {
 
-const void* sample_kernel_f32(int nt) {
-  (void)nt;
-  return reinterpret_cast<const void*>(&stream_kernel<false>);
-}
+const void* sample_kernel_f32() { return reinterpret_cast<const void*>(&sample_kernel<false>); }
 
 }  // namespace sv

@@ -8,11 +8,23 @@
 namespace sv {
 
 constexpr int kChunk = 8;         // logits held per register chunk
-constexpr int kNV = 4;            // chunks per thread per row
 constexpr int kMaxCluster = 16;   // CTAs that share one row (non-portable cluster size)
 constexpr int kMaxK = 31;         // drafted positions per request (lanes 0..K of one warp in the cut)
-constexpr int kTileLogits = 32 * kNV * kChunk;   // greedy path: logits per warp tile
-constexpr int kStreamStagesHost = 4;              // sampling path: items in each thread's copy pipeline
+// Sampling kernel geometry: 8 warps per CTA; per item every lane holds kSampPieces 16-byte pieces
+// of each row; each warp streams its own bytes through a ring of kSampStages items.
+#ifndef SPEC_SAMP_PIECES
+#define SPEC_SAMP_PIECES 2
+#endif
+#ifndef SPEC_SAMP_STAGES
+#define SPEC_SAMP_STAGES 4
+#endif
+constexpr int kSampWarps = 8;
+constexpr int kSampPieces = SPEC_SAMP_PIECES;
+constexpr int kSampStages = SPEC_SAMP_STAGES;
+constexpr int kSampWarpBytes = kSampPieces * 512;                    // one row, one item, one warp
+constexpr int kSampItemBytes = kSampWarps * kSampWarpBytes;           // one row, one item
+constexpr int kSampRingBytes = kSampStages * 2 * kSampItemBytes;      // dynamic shared memory per CTA
+constexpr int kSampMaxItems = 32;                                     // items per slice
 
 // Status bits in the workspace's device status word.
 constexpr int kStatusTimeout = 1;
@@ -46,7 +58,7 @@ struct ArgmaxParams {
   int drows;                 // draft rows scanned per request (K when the one-hot alpha is wanted)
   int tpr;                   // tiles per row
   long long total_tiles;     // B * (rows_t + drows) * tpr
-  int aligned;               // rows start on 16-byte boundaries (bulk-copy ring)
+  int aligned;               // rows start on 16-byte boundaries: 16-byte vector loads
   long long wait_limit;      // ns of wall time per bounded wait; 0 = give up at once
   int fused_cut;             // the warp that completes a request runs its cut
   int stats_only;            // overlap statistics only (no tokens)
@@ -55,7 +67,7 @@ struct ArgmaxParams {
 enum : int {
   F_NEED_DRAFT = 1,   // draft rows are read for positions k < K
   F_STATS_ONLY = 2,   // rows k < K only; alpha, no draws
-  F_TMA = 8,          // rows are 16-byte aligned: bulk-copy staging ring
+  F_ALIGNED = 8,      // rows start on 16-byte boundaries: staged by 1-D bulk copies
   F_ALL_PDRAWS = 16,  // draw from p at every row (the verified depth is chosen afterwards)
 };
 
@@ -76,8 +88,6 @@ struct RowParams {
   int U;                     // rows (units) per request: K+1, or K in stats-only mode
   int total_units;           // B * U
   int slice;                 // logits per CTA slice (multiple of kChunk)
-  int nstage;                // copy pipeline depth in items (aligned rows)
-  int stage_row_bytes;       // bytes per row slot in a stage (multiple of 128)
   int flags;
   float c;                   // log2(e) / T  (T > 0)
   long long wait_limit;      // ns of wall time per bounded wait; 0 = give up at once
@@ -105,7 +115,7 @@ struct BudgetParams {
 
 // Host-side launchers of the small kernels (defined next to them).
 cudaError_t launch_argmax(bool bf16, const ArgmaxParams& p, int grid, cudaStream_t stream);
-cudaError_t argmax_blocks_per_sm(bool bf16, int nstage, int* out);
+cudaError_t argmax_blocks_per_sm(bool bf16, int* out);
 cudaError_t launch_budget_cut(const BudgetParams& p, cudaStream_t stream);
 cudaError_t launch_cut(const BudgetParams& p, const int32_t* depth, cudaStream_t stream);
 

@@ -81,7 +81,7 @@ extern "C" spec_status_t spec_verify_chain_greedy_static(const void* target_logi
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SPEC_ERR_CUDA;
-  if (sv::argmax_blocks_per_sm(dtype == SPEC_BF16, 0, &per_sm) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (sv::argmax_blocks_per_sm(dtype == SPEC_BF16, &per_sm) != cudaSuccess) return SPEC_ERR_CUDA;
 
   sv::ArgmaxParams p = {};
   p.target = target_logits;

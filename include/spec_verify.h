@@ -206,32 +206,49 @@ spec_status_t spec_verify_chain_greedy_static(const void* target_logits, const v
                                               int32_t* out_status, void* stream);
 
 /*
- * Test hook: wall-time limit, in microseconds, of every bounded on-device
- * wait (default 200000, i.e. 200 ms; measured with the GPU's global timer).
- * 0 makes every such wait give up at once, which sets
- * SPEC_ERR_DEVICE_TIMEOUT; copies already issued are still drained (up to
- * 100 ms each) before a kernel returns.  Negative restores the default.
- * Process-wide; not for production use.
+ * Test and tuning knobs of one call (no process-wide settings exist).  A
+ * zero-filled struct means the defaults everywhere.
+ *   wait_limit_us   0: default wall-time limit of every bounded on-device wait
+ *                   (200 ms, read from the GPU's global timer); > 0: that
+ *                   limit; < 0: every such wait gives up at once, which sets
+ *                   SPEC_ERR_DEVICE_TIMEOUT in the status word (the kernel
+ *                   then waits once more, up to 100 ms, so its copies and
+ *                   cluster exchanges still complete before it returns).
+ *   cluster         T > 0: CTAs per row of the sampling kernel (1, 2, 4, 8 or
+ *                   16; a slice must not exceed 32 items of 8 KB per row, else
+ *                   SPEC_ERR_UNSUPPORTED); 0: chosen per call shape.
+ *   greedy_variant  T == 0: bit 1 runs the cut in its own kernel instead of
+ *                   fusing it into the argmax kernel; bit 2 launches every
+ *                   resident CTA slot with the tiles spread evenly.
+ *   plan_out        host int32[8] or NULL: receives the launched plan,
+ *                   sampling kernel {threads, cluster, clusters launched, max
+ *                   co-resident clusters, slice, ring stages, ring bytes,
+ *                   flags}; argmax kernel {threads, 1, grid, resident CTAs,
+ *                   tile, 0, 0, -1}.
  */
-void spec_debug_set_wait_limit(long long limit_us);
+typedef struct spec_tuning {
+  long long wait_limit_us;
+  int cluster;
+  int greedy_variant;
+  int32_t* plan_out;
+} spec_tuning_t;
 
 /*
- * Tuning hooks (process-wide, not for production use).  spec_debug_set_plan
- * forces the sampling row kernel's cluster size (CTAs per row, 1..16; the
- * cluster must cover V with 32 items of 4096 logits, else the call returns
- * SPEC_ERR_UNSUPPORTED); 0 keeps the automatic choice.  `threads` and
- * `nstage` are accepted for compatibility and ignored (the kernel runs 256
- * threads per CTA and a fixed copy pipeline).  spec_debug_last_plan writes
- * the last launched plan: sampling kernel {threads, cluster, clusters
- * launched, max co-resident clusters, slice, stages, ring bytes, flags};
- * argmax kernel {threads, 1, grid, resident CTAs, tile, 0, 0, -1}.
+ * spec_verify_block with per-call knobs (tuning may be NULL = defaults).
+ * stats_only != 0 computes what spec_overlap_alpha computes (tokens,
+ * uniforms, depth, budget_N, out_tokens, out_accepted and out_depth are then
+ * ignored).  Same argument meaning, ownership and errors as those calls;
+ * SPEC_ERR_INVALID_ARG for a cluster size that is not a power of two in
+ * [1, 16].
  */
-void spec_debug_set_plan(int threads, int cluster, int nstage);
-/* Greedy-path schedule variant: bit 1 runs the cut in a separate kernel (0 = fused, default);
- * bit 2 launches every resident CTA slot, the tiles spread evenly over the warps (default: the
- * fewest CTAs that give every warp the same number of tiles). */
-void spec_debug_set_variant(int variant);
-void spec_debug_last_plan(int32_t* out8);
+spec_status_t spec_verify_tuned(const void* target_logits, const void* draft_logits, int dtype,
+                                const int32_t* tokens, const float* uniforms,
+                                int B, int K, int V, float temperature,
+                                const int32_t* depth, int budget_N, int stats_only,
+                                int32_t* out_tokens, int32_t* out_accepted, float* out_alpha,
+                                float* out_cum_alpha, float* out_expected_len, int32_t* out_depth,
+                                void* workspace, size_t ws_bytes, void* stream,
+                                const spec_tuning_t* tuning);
 
 #ifdef __cplusplus
 }
