@@ -15,8 +15,8 @@
 #include "spec_internal.h"
 
 namespace sv {
-const void* sample_kernel_bf16();
-const void* sample_kernel_f32();
+const void* sample_kernel_bf16(bool aligned);
+const void* sample_kernel_f32(bool aligned);
 }  // namespace sv
 
 namespace {
@@ -38,26 +38,28 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Workspace layout, a function of the buffer size only (so the greedy keys, which the cut
 // kernel clears after every call, never overlap bytes another call shape wrote):
 //   [status word | pad to 256] [argmax keys: cap rows x 16 B] [request counters: cap x 4 B]
-//   [row records: cap rows x 32 B]
+//   [row records: cap rows x 32 B] [row mass tables: cap rows x kMassRowFloats x 4 B]
 // where cap = the number of (request, position) rows the buffer can hold.
 constexpr size_t kKeyBytes = 2 * sizeof(uint64_t);
-constexpr size_t kRowBytes = kKeyBytes + sizeof(int32_t) + sizeof(UnitRec);
+constexpr size_t kMassBytes = sizeof(float) * sv::kMassRowFloats;
+constexpr size_t kRowBytes = kKeyBytes + sizeof(int32_t) + sizeof(UnitRec) + kMassBytes;
 struct WsLayout {
-  size_t status, keys, counters, recs, cap_rows;
+  size_t status, keys, counters, recs, mass, cap_rows;
 };
 WsLayout ws_layout_for(size_t ws_bytes) {
   WsLayout L;
   L.status = 0;
   L.keys = kAlign;
-  const size_t avail = ws_bytes > 4 * kAlign ? ws_bytes - 4 * kAlign : 0;
+  const size_t avail = ws_bytes > 5 * kAlign ? ws_bytes - 5 * kAlign : 0;
   L.cap_rows = avail / kRowBytes;
   L.counters = align_up(L.keys + L.cap_rows * kKeyBytes, kAlign);
   L.recs = align_up(L.counters + L.cap_rows * sizeof(int32_t), kAlign);
+  L.mass = align_up(L.recs + L.cap_rows * sizeof(UnitRec), kAlign);
   return L;
 }
 size_t ws_bytes_needed(int B, int K) {
   const size_t rows = static_cast<size_t>(B > 0 ? B : 1) * (K + 1);
-  return 4 * kAlign + rows * kRowBytes;
+  return 5 * kAlign + rows * kRowBytes;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -163,21 +165,22 @@ struct RowPlan {
   RowParams p;
 };
 
-// Estimated duration (arbitrary units) of the sampling kernel with clusters of C CTAs: the units
-// go round-robin to the clusters (pairs first), every unit streams its rows twice (HBM, then L2)
-// and pays a fixed cost for its two cluster exchanges and draws.
-double plan_cost(int C, int ncl, int npairs, int nsingle, double row_bytes, int resident_slots) {
+// Estimated duration (seconds) of the sampling kernel with clusters of C CTAs: units go
+// round-robin to the clusters (pairs first); a CTA streams its slice of a unit's rows at its
+// share of the HBM bandwidth (pass 2 overlaps the next unit's pass 1), and every step pays a
+// fixed cost for the cluster exchange and the normalisers.  The constants were fitted to timings
+// of the verification configurations on a GB300 (effective 3 TB/s shared by the CTAs, at most
+// 15 GB/s per CTA, 2 us per step).
+double plan_cost(int C, int ncl, int npairs, int nsingle, double row_bytes) {
   const int units = npairs + nsingle;
   if (ncl < 1) return 1e300;
-  // per-CTA bandwidth: the HBM shared by the active CTAs, capped by what one CTA's copy ring sustains
-  const double active = static_cast<double>(ncl) * C;
-  const double bw = std::fmin(6.5e12 / std::fmin(active, resident_slots), 3.0e10);
-  const double t_row = 1.5 * row_bytes / C / bw;        // two passes, the second from L2
-  const double t_unit = 2.0e-6;                         // exchanges, draws
+  const double bw = std::fmin(3.0e12 / (static_cast<double>(ncl) * C), 1.5e10);
+  const double t_row = row_bytes / C / bw;
+  const double t_step = 2.0e-6;
   double worst = 0.0;
   for (int j = 0; j < ncl && j < units; ++j) {
-    double t = 0.0;
-    for (int u = j; u < units; u += ncl) t += (u < npairs ? 2.0 : 1.0) * t_row + t_unit;
+    double t = t_step;
+    for (int u = j; u < units; u += ncl) t += (u < npairs ? 2.0 : 1.0) * t_row + t_step;
     worst = std::fmax(worst, t);
   }
   return worst;
@@ -187,7 +190,9 @@ spec_status_t plan_rows(const void* target, const void* draft, int dtype, int B,
                         bool need_draft, bool stats_only, const Knobs& kn, RowPlan* plan) {
   const bool bf16 = dtype == SPEC_BF16;
   const int esz = bf16 ? 2 : 4;
-  const void* fn = bf16 ? sv::sample_kernel_bf16() : sv::sample_kernel_f32();
+  const bool aligned = (static_cast<size_t>(V) * esz) % 16 == 0 && aligned16(target) &&
+                       (!need_draft || aligned16(draft));
+  const void* fn = bf16 ? sv::sample_kernel_bf16(aligned) : sv::sample_kernel_f32(aligned);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
   int sms = 0;
@@ -208,8 +213,8 @@ spec_status_t plan_rows(const void* target, const void* draft, int dtype, int B,
     if (it != g_plans.end()) std::tie(best_c, best_ncl, best_maxc) = it->second;
   }
   if (best_c == 0) {
-    // the bytes streamed between a logit's first and second read must fit in about half the L2,
-    // or the second pass goes back to HBM; among the sizes that keep it there, the cheapest
+    // the bytes streamed between a logit's first and second read must fit in the L2 with room to
+    // spare, or the second pass goes back to HBM; among the sizes that keep it there, the cheapest
     // estimated schedule wins (the largest size if none does)
     bool best_fits = false;
     double best = 1e300;
@@ -221,8 +226,8 @@ spec_status_t plan_rows(const void* target, const void* draft, int dtype, int B,
       if (maxc < 1) continue;
       const int ncl = units < maxc ? units : maxc;
       const double window = static_cast<double>(ncl) * (need_draft ? 2.0 : 1.0) * row_bytes;
-      const bool fits = kn.cluster != 0 || window <= 0.5 * static_cast<double>(l2);
-      const double cost = plan_cost(C, ncl, npairs, nsingle, row_bytes, maxc * C);
+      const bool fits = kn.cluster != 0 || window <= 0.75 * static_cast<double>(l2);
+      const double cost = plan_cost(C, ncl, npairs, nsingle, row_bytes);
       const bool better = (fits && !best_fits) || (fits == best_fits && (fits ? cost < best * 0.97 : C > best_c));
       if (best_c == 0 || better) {
         best = cost;
@@ -240,8 +245,9 @@ spec_status_t plan_rows(const void* target, const void* draft, int dtype, int B,
   int slice = (V + best_c - 1) / best_c;
   slice = static_cast<int>(align_up(slice, sv::kChunk));
   if (static_cast<long long>(slice) * esz > static_cast<long long>(kMaxItems) * kItemBytes) return SPEC_ERR_UNSUPPORTED;
-  const bool aligned = (static_cast<size_t>(V) * esz) % 16 == 0 && aligned16(target) &&
-                       (!need_draft || aligned16(draft));
+  const int item_logits = kItemBytes / esz;
+  const int itmax = (slice + item_logits - 1) / item_logits;
+  if (best_c * itmax > sv::kMassMaxSegments) return SPEC_ERR_UNSUPPORTED;
   plan->fn = fn;
   plan->cluster = best_c;
   plan->nclusters = best_ncl;
@@ -256,6 +262,7 @@ spec_status_t plan_rows(const void* target, const void* draft, int dtype, int B,
   p.U = stats_only ? K : K + 1;
   p.total_units = units;
   p.slice = slice;
+  p.itmax = itmax;
   p.flags = (need_draft ? sv::F_NEED_DRAFT : 0) | (stats_only ? sv::F_STATS_ONLY : 0) |
             (aligned ? sv::F_ALIGNED : 0);
   p.c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
@@ -353,6 +360,19 @@ spec_status_t check_ws(void* ws, size_t ws_bytes, int B, int K) {
   return SPEC_OK;
 }
 
+// What the cut kernels need to read the sampling kernel's records and redo its one draw.
+void set_sampling_geometry(sv::BudgetParams* bp, const RowPlan& plan, const float* mass, int dtype) {
+  bp->mass = mass;
+  bp->target = plan.p.target;
+  bp->draft = plan.p.draft;
+  bp->c = plan.p.c;
+  bp->bf16 = dtype == SPEC_BF16;
+  bp->aligned = (plan.p.flags & sv::F_ALIGNED) != 0;
+  bp->ncta = plan.cluster;
+  bp->slice = plan.p.slice;
+  bp->itmax = plan.p.itmax;
+}
+
 struct VerifyArgs {
   const void* target;
   const void* draft;
@@ -395,9 +415,12 @@ spec_status_t run_verify(const VerifyArgs& a, const Knobs& kn) {
   const WsLayout L = ws_layout_for(a.ws_bytes);
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
   UnitRec* recs = reinterpret_cast<UnitRec*>(ws + L.recs);
+  float* mass = reinterpret_cast<float*>(ws + L.mass);
   uint64_t* keys = reinterpret_cast<uint64_t*>(ws + L.keys);
   int32_t* counters = reinterpret_cast<int32_t*>(ws + L.counters);
   int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
+  RowPlan plan;
+  std::memset(&plan, 0, sizeof(plan));
   if (greedy) {
     sv::ArgmaxParams cut;
     std::memset(&cut, 0, sizeof(cut));
@@ -415,7 +438,6 @@ spec_status_t run_verify(const VerifyArgs& a, const Knobs& kn) {
     if (st != SPEC_OK) return st;
     if (!budget && (kn.variant & 2) == 0) return SPEC_OK;   // the cut ran inside the argmax kernel
   } else {
-    RowPlan plan;
     st = plan_rows(a.target, a.draft, a.dtype, a.B, a.K, a.V, a.T, need_draft, false, kn, &plan);
     if (st != SPEC_OK) return st;
     RowParams& p = plan.p;
@@ -423,6 +445,7 @@ spec_status_t run_verify(const VerifyArgs& a, const Knobs& kn) {
     p.uniforms = a.uniforms;
     p.depth = a.depth;
     p.recs = recs;
+    p.mass = mass;
     p.status = status;
     if (budget) p.flags |= sv::F_ALL_PDRAWS;
     st = launch_plan(&plan, kn, a.stream);
@@ -452,6 +475,7 @@ spec_status_t run_verify(const VerifyArgs& a, const Knobs& kn) {
   bp.out_cum = a.out_cum;
   bp.out_E = a.out_E;
   bp.status = status;
+  set_sampling_geometry(&bp, plan, mass, a.dtype);
   const cudaError_t e = budget ? sv::launch_budget_cut(bp, a.stream) : sv::launch_cut(bp, a.depth, a.stream);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
@@ -469,9 +493,12 @@ spec_status_t run_overlap(const void* target_logits, const void* draft_logits, i
   const WsLayout L = ws_layout_for(ws_bytes);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   UnitRec* recs = reinterpret_cast<UnitRec*>(ws + L.recs);
+  float* mass = reinterpret_cast<float*>(ws + L.mass);
   uint64_t* keys = reinterpret_cast<uint64_t*>(ws + L.keys);
   int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
   const bool greedy = temperature == 0.f;
+  RowPlan plan;
+  std::memset(&plan, 0, sizeof(plan));
   if (greedy) {
     sv::ArgmaxParams cut;
     std::memset(&cut, 0, sizeof(cut));
@@ -483,10 +510,10 @@ spec_status_t run_overlap(const void* target_logits, const void* draft_logits, i
     st = launch_greedy(target_logits, draft_logits, dtype, B, K, V, true, true, true, keys, cut, kn, stream);
     if (st != SPEC_OK || (kn.variant & 2) == 0) return st;
   } else {
-    RowPlan plan;
     st = plan_rows(target_logits, draft_logits, dtype, B, K, V, temperature, true, true, kn, &plan);
     if (st != SPEC_OK) return st;
     plan.p.recs = recs;
+    plan.p.mass = mass;
     plan.p.status = status;
     st = launch_plan(&plan, kn, stream);
   }
@@ -506,6 +533,7 @@ spec_status_t run_overlap(const void* target_logits, const void* draft_logits, i
   bp.out_cum = out_cum_alpha;
   bp.out_E = out_expected_len;
   bp.status = status;
+  set_sampling_geometry(&bp, plan, mass, dtype);
   return sv::launch_cut(bp, nullptr, stream) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

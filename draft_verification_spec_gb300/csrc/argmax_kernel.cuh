@@ -227,9 +227,8 @@ __global__ void __launch_bounds__(256, BF16 ? 4 : 2) argmax_kernel(const __grid_
     if (old + cnt == tiles_req) {                      // this warp finished request `req`
       __syncwarp();   // lane 0's acquire, then the warp barrier: every lane's loads see the keys
       const int d = P.depth ? min(max(P.depth[req], 0), K) : K;
-      cut_request(req, d, true, P.stats_only != 0, nullptr, P.keys, P.drows > 0, true, P.rows_t, K, V,
-                  P.tokens, nullptr, P.out_tokens, P.out_accepted, P.out_alpha, P.out_cum, P.out_E,
-                  P.status, lane);
+      cut_request(req, d, P.stats_only != 0, P.keys, P.drows > 0, true, P.rows_t, K, V, P.tokens,
+                  P.out_tokens, P.out_accepted, P.out_alpha, P.out_cum, P.out_E, P.status, lane);
       if (lane == 0) P.counters[req] = 0;
     }
   };

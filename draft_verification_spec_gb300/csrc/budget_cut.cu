@@ -4,11 +4,12 @@
 //    prod_{k<=m} alpha_k, prefix-closed per request -- then the cut at the chosen depths.
 // Both start with griddepcontrol.wait, so they may be scheduled while the row kernel drains.
 #include "argmax_kernel.cuh"
+#include "cut_sampling.cuh"
 #include "spec_device.cuh"
 
 namespace sv {
 
-constexpr int kBudgetThreads = 1024;
+constexpr int kBudgetThreads = 512;
 constexpr int kCutThreads = 128;
 
 // key (c2, m2, b2) precedes key (c, m, b): c descending, then m ascending, then b ascending
@@ -18,12 +19,9 @@ __device__ __forceinline__ bool precedes(float c2, int m2, int b2, float c, int 
 
 __device__ __forceinline__ float alpha_of(const BudgetParams& P, int b, int k) {
   if (P.alpha_in) return P.alpha_in[static_cast<size_t>(b) * P.K + k];
-  if (P.greedy) {
-    const unsigned long long* kb = reinterpret_cast<const unsigned long long*>(P.keys) +
-                                   (static_cast<size_t>(b) * (P.K + 1) + k) * 2;
-    return key_index(__ldcg(kb)) == key_index(__ldcg(kb + 1)) ? 1.f : 0.f;
-  }
-  return __ldcg(&P.recs[static_cast<size_t>(b) * P.U + k].alpha);
+  const unsigned long long* kb = reinterpret_cast<const unsigned long long*>(P.keys) +
+                                 (static_cast<size_t>(b) * (P.K + 1) + k) * 2;
+  return key_index(__ldcg(kb)) == key_index(__ldcg(kb + 1)) ? 1.f : 0.f;
 }
 
 // One CTA builds the whole confidence table; its warps take requests b = warp, warp + nwarps, ...
@@ -32,16 +30,29 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid
   extern __shared__ float conf[];   // [B, K] prefix confidences
   asm volatile("griddepcontrol.wait;" ::: "memory");   // the row kernel's results are complete
   const int B = P.B, K = P.K;
-  for (int b = threadIdx.x; b < B; b += blockDim.x) {
-    float cp = 1.f;
-    for (int k = 0; k < K; ++k) {
-      cp *= fminf(fmaxf(alpha_of(P, b, k), 0.f), 1.f);   // clamp; NaN -> 0
-      conf[b * K + k] = cp;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;
+  if (P.alpha_in || P.greedy) {
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+      float cp = 1.f;
+      for (int k = 0; k < K; ++k) {
+        cp *= fminf(fmaxf(alpha_of(P, b, k), 0.f), 1.f);   // clamp; NaN -> 0
+        conf[b * K + k] = cp;
+      }
+    }
+  } else {
+    // sampling path: every row's alpha in parallel (a thread per row), then the prefix products
+    for (int r = threadIdx.x; r < B * K; r += blockDim.x) conf[r] = alpha_of_row(P, r / K, r - (r / K) * K);
+    __syncthreads();
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+      float cp = 1.f;
+      for (int k = 0; k < K; ++k) {
+        cp *= conf[b * K + k];
+        conf[b * K + k] = cp;
+      }
     }
   }
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nw = blockDim.x >> 5;
   for (int b = blockIdx.x * nw + warp; b < B; b += gridDim.x * nw) {
     // rank of key (b, m): within each request b' the keys that precede it form a prefix
     // (conf is non-increasing in m'), found by binary search; lanes split the requests.
@@ -68,10 +79,13 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid
     if (P.out_depth && lane == 0) P.out_depth[b] = d;
     if (P.out_conf)
       for (int k = lane; k < K; k += 32) P.out_conf[static_cast<size_t>(b) * K + k] = conf[b * K + k];
-    if (P.do_cut)
-      cut_request(b, d, P.greedy != 0, P.stats_only != 0, P.recs, P.keys, P.draft_keys != 0, false, P.U, K,
-                  P.V, P.tokens, P.uniforms, P.out_tokens, P.out_accepted, P.out_alpha, P.out_cum, P.out_E,
-                  P.status, lane);
+    if (P.do_cut) {
+      if (P.greedy)
+        cut_request(b, d, P.stats_only != 0, P.keys, P.draft_keys != 0, false, P.U, K, P.V, P.tokens,
+                    P.out_tokens, P.out_accepted, P.out_alpha, P.out_cum, P.out_E, P.status, lane);
+      else
+        cut_sampling(P, b, d, lane);
+    }
   }
   if (P.greedy && P.keys) {   // every warp of the (single) CTA is done with the keys: clear them
     __syncthreads();
@@ -87,9 +101,11 @@ __global__ void __launch_bounds__(kCutThreads) cut_kernel(const __grid_constant_
   const int b = blockIdx.x * (kCutThreads / 32) + warp;
   if (b >= P.B) return;
   const int d = depth ? min(max(depth[b], 0), P.K) : P.K;
-  cut_request(b, d, P.greedy != 0, P.stats_only != 0, P.recs, P.keys, P.draft_keys != 0, true, P.U, P.K,
-              P.V, P.tokens, P.uniforms, P.out_tokens, P.out_accepted, P.out_alpha, P.out_cum, P.out_E,
-              P.status, lane);
+  if (P.greedy)
+    cut_request(b, d, P.stats_only != 0, P.keys, P.draft_keys != 0, true, P.U, P.K, P.V, P.tokens,
+                P.out_tokens, P.out_accepted, P.out_alpha, P.out_cum, P.out_E, P.status, lane);
+  else
+    cut_sampling(P, b, d, lane);
 }
 
 // Launch chained to the previous kernel on the stream (programmatic dependent launch): the

@@ -101,27 +101,10 @@ __device__ __forceinline__ int select_lane(float mass, float cum0, float t, bool
 __device__ __forceinline__ float ldcg_f(const float* p) { return __ldcg(p); }
 __device__ __forceinline__ int ldcg_i(const int32_t* p) { return __ldcg(p); }
 
-// Serial-acceptance cut of one request, run by one whole warp (lane k <-> position k).
-// Sampling path: reads the per-row records; greedy path: resolves the argmax keys (and clears
-// them for the next call when `clear_keys`).  d = verified depth in [0, K].
-__device__ __forceinline__ void cut_request(int b, int d, bool greedy, bool stats_only,
-                                            const UnitRec* recs, uint64_t* keys, bool draft_keys,
-                                            bool clear_keys, int U, int K, int V,
-                                            const int32_t* tokens, const float* uniforms,
-                                            int32_t* out_tokens, int32_t* out_accepted,
-                                            float* out_alpha, float* out_cum, float* out_E,
-                                            int32_t* status, int lane) {
-  const UnitRec* r = recs + static_cast<size_t>(b) * U;
-  uint64_t* kb = keys + static_cast<size_t>(b) * (K + 1) * 2;
-  // greedy: argmax of the target row at this lane's position (and of the draft row)
-  int g = -1, gd = -2;
-  if (greedy && lane < U) {
-    g = key_index(__ldcg(reinterpret_cast<const unsigned long long*>(kb) + 2 * lane));
-    if (draft_keys && lane < K) gd = key_index(__ldcg(reinterpret_cast<const unsigned long long*>(kb) + 2 * lane + 1));
-  }
-  // alpha, prefix confidences (left-to-right fp32 product) and expected length
-  float a = 0.f;
-  if (lane < K) a = greedy ? (draft_keys && g == gd ? 1.f : 0.f) : ldcg_f(&r[lane].alpha);
+// Alpha, prefix confidences and expected length of one request from this lane's alpha (lane k
+// holds alpha_k, k < K): left-to-right fp32 products, written where requested.
+__device__ __forceinline__ void write_stats(int b, int K, float a, float* out_alpha, float* out_cum,
+                                            float* out_E, int lane) {
   if (out_alpha && lane < K) out_alpha[static_cast<size_t>(b) * K + lane] = a;
   if (out_cum || out_E) {
     float cprod = 1.f, esum = 0.f, mine = 0.f;
@@ -133,6 +116,25 @@ __device__ __forceinline__ void cut_request(int b, int d, bool greedy, bool stat
     if (out_cum && lane < K) out_cum[static_cast<size_t>(b) * K + lane] = mine;
     if (out_E && lane == 0) out_E[b] = esum;
   }
+}
+
+// Greedy serial-acceptance cut of one request, run by one whole warp (lane k <-> position k):
+// resolves the argmax keys (and clears them for the next call when `clear_keys`).  d = verified
+// depth in [0, K].
+__device__ __forceinline__ void cut_request(int b, int d, bool stats_only, uint64_t* keys, bool draft_keys,
+                                            bool clear_keys, int U, int K, int V, const int32_t* tokens,
+                                            int32_t* out_tokens, int32_t* out_accepted, float* out_alpha,
+                                            float* out_cum, float* out_E, int32_t* status, int lane) {
+  uint64_t* kb = keys + static_cast<size_t>(b) * (K + 1) * 2;
+  // argmax of the target row at this lane's position (and of the draft row)
+  int g = -1, gd = -2;
+  if (lane < U) {
+    g = key_index(__ldcg(reinterpret_cast<const unsigned long long*>(kb) + 2 * lane));
+    if (draft_keys && lane < K) gd = key_index(__ldcg(reinterpret_cast<const unsigned long long*>(kb) + 2 * lane + 1));
+  }
+  // the one-hot alpha: 1 where the target and draft argmaxes agree
+  const float a = (lane < K && draft_keys && g == gd) ? 1.f : 0.f;
+  write_stats(b, K, a, out_alpha, out_cum, out_E, lane);
   if (!stats_only) {
     bool ok = true;
     int x = -1;
@@ -141,28 +143,18 @@ __device__ __forceinline__ void cut_request(int b, int d, bool greedy, bool stat
       if (x < 0 || x >= V) {
         ok = false;
         atomicOr(status, kStatusTokenRange);
-      } else if (greedy) {
-        ok = (x == g);
       } else {
-        const float u = uniforms[static_cast<size_t>(b) * (K + 1) + lane];
-        ok = u * ldcg_f(&r[lane].qx) < ldcg_f(&r[lane].px);
+        ok = (x == g);
       }
     }
     const unsigned rej = __ballot_sync(0xffffffffu, lane < d && !ok);
     const int n = rej ? __ffs(rej) - 1 : d;
-    int tok = -1;
-    if (greedy) {
-      tok = __shfl_sync(0xffffffffu, g, n);
-    } else if (lane == 0) {
-      if (n < d) tok = (ldcg_f(&r[n].R) > 0.f) ? ldcg_i(&r[n].rs) : ldcg_i(&r[n].ps);
-      else tok = ldcg_i(&r[n].ps);
-    }
-    tok = __shfl_sync(0xffffffffu, tok, 0);
+    const int tok = __shfl_sync(0xffffffffu, g, n);
     int32_t* ot = out_tokens + static_cast<size_t>(b) * (K + 1);
     for (int i = lane; i <= K; i += 32) ot[i] = (i < n) ? x : (i == n ? tok : -1);
     if (lane == 0) out_accepted[b] = n;
   }
-  if (greedy && clear_keys && lane < U) {
+  if (clear_keys && lane < U) {
     kb[2 * lane] = 0ull;
     kb[2 * lane + 1] = 0ull;
   }

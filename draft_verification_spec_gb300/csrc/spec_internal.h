@@ -10,33 +10,52 @@ namespace sv {
 constexpr int kChunk = 8;         // logits held per register chunk
 constexpr int kMaxCluster = 16;   // CTAs that share one row (non-portable cluster size)
 constexpr int kMaxK = 31;         // drafted positions per request (lanes 0..K of one warp in the cut)
-// Sampling kernel geometry: 8 warps per CTA; per item every lane holds kSampPieces 16-byte pieces
-// of each row; each warp streams its own bytes through a ring of kSampStages items.
+// Sampling kernel geometry: 8 warps per CTA; per item every lane loads kSampPieces 16-byte pieces
+// of each row straight into registers.
 #ifndef SPEC_SAMP_PIECES
 #define SPEC_SAMP_PIECES 2
 #endif
+#ifndef SPEC_SAMP_MINB
+#define SPEC_SAMP_MINB 2
+#endif
 #ifndef SPEC_SAMP_STAGES
-#define SPEC_SAMP_STAGES 4
+#define SPEC_SAMP_STAGES 3
 #endif
 constexpr int kSampWarps = 8;
 constexpr int kSampPieces = SPEC_SAMP_PIECES;
-constexpr int kSampStages = SPEC_SAMP_STAGES;
 constexpr int kSampWarpBytes = kSampPieces * 512;                    // one row, one item, one warp
 constexpr int kSampItemBytes = kSampWarps * kSampWarpBytes;           // one row, one item
-constexpr int kSampRingBytes = kSampStages * 2 * kSampItemBytes;      // dynamic shared memory per CTA
 constexpr int kSampMaxItems = 32;                                     // items per slice
+constexpr int kSampMinBlocks = SPEC_SAMP_MINB;                        // resident CTAs per SM the registers allow
+// Aligned rows are staged through each warp's ring of kSampStages stages, a stage holding the
+// warp's bytes of one item of four rows (pass-1 target, draft; pass-2 target, draft).
+constexpr int kSampStages = SPEC_SAMP_STAGES;
+constexpr int kSampRingBytes = kSampWarps * kSampStages * 4 * kSampWarpBytes;   // dynamic shared memory
 
 // Status bits in the workspace's device status word.
 constexpr int kStatusTimeout = 1;
 constexpr int kStatusTokenRange = 2;
 
-// Per (request, position) results of the sampling row kernel; 32 bytes.
+// Per (request, position) results of the sampling row kernel; 32 bytes.  Written by CTA 0 of the
+// unit's cluster once the row normalisers are known.
 struct UnitRec {
   float px, qx;      // p_k(x_k), q_k(x_k)
-  float alpha, R;    // overlap sum min(p,q) and residual mass sum max(0, p-q)
-  int32_t rs, ps;    // residual draw, draw from p (bonus candidate); -1 if none
-  int32_t pad0, pad1;
+  float offt, offd;  // p_v = 2^(z_T[v] c - offt), q_v = 2^(z_D[v] c - offd)
+  int32_t mode;      // pass-2 work done: kModeAlpha, kModeFull or kModeSingle
+  int32_t pad0, pad1, pad2;
 };
+enum : int32_t { kModeAlpha = 0, kModeFull = 1, kModeSingle = 2 };
+
+// Per-row mass table of the sampling kernel, written by every warp of every CTA of the unit's
+// cluster (floats):
+//   a[c * 8 + w]                       alpha partial of warp w of CTA c (sum min(p, q))
+//   m[((c * itmax + it) * 8 + w) * 2]  (R, P): residual mass sum max(0, p - q) and mass sum p of
+//                                      item `it` of warp w of CTA c (full / single rows)
+// in vocabulary order (c, it, w).  The cut kernels sum alpha and draw from these.
+constexpr int kMassAlphaFloats = 16 * 8;                 // clusters of up to 16 CTAs x 8 warps
+constexpr int kMassMaxSegments = 80;                     // CTA x item segments of a row (V * e / 8 KB + 16)
+constexpr int kMassRowFloats = kMassAlphaFloats + kMassMaxSegments * 8 * 2;
+
 // Greedy path: per (request, position) two 64-bit argmax keys (target row, draft row), folded
 // with atomicMax by the argmax kernel and cleared by the kernel that consumes them.
 
@@ -83,11 +102,13 @@ struct RowParams {
   float* out_cum;            // [B, K] or null
   float* out_E;              // [B] or null
   UnitRec* recs;             // [B, U]
+  float* mass;               // [B, U] mass tables of kMassRowFloats
   int32_t* status;           // 1 word
   int B, K, V;
   int U;                     // rows (units) per request: K+1, or K in stats-only mode
   int total_units;           // B * U
   int slice;                 // logits per CTA slice (multiple of kChunk)
+  int itmax;                 // items of the first (longest) slice
   int flags;
   float c;                   // log2(e) / T  (T > 0)
   long long wait_limit;      // ns of wall time per bounded wait; 0 = give up at once
@@ -96,6 +117,12 @@ struct RowParams {
 struct BudgetParams {
   const float* alpha_in;     // [B, K] caller alpha, or null: from recs / keys
   const UnitRec* recs;
+  const float* mass;         // sampling path: [B, U] mass tables
+  const void* target;        // sampling path: logits, for the one draw per request
+  const void* draft;
+  float c;                   // log2(e) / T
+  int bf16, aligned;         // logits element type; rows start on 16-byte boundaries
+  int ncta, slice, itmax;    // the sampling kernel's cluster size, slice and items per slice
   uint64_t* keys;            // greedy path: argmax keys [B, K+1, 2] (cleared after use)
   int draft_keys;            // greedy path: draft keys were produced (one-hot alpha)
   int U;
