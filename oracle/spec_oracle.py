@@ -126,6 +126,8 @@ class VerifyResult:
     expected_len: np.ndarray  # [B] float64
     margin: np.ndarray        # [B] float64: smallest decision margin up to the cut
     depth: np.ndarray         # [B] int64 depth used
+    margin_accept: Optional[np.ndarray] = None   # [B] smallest |u_k - p_k(x_k)/q_k(x_k)| over tested k
+    margin_cdf: Optional[np.ndarray] = None      # [B] boundary distance of the final draw
 
 
 def _first_false(ok: np.ndarray, d: np.ndarray) -> np.ndarray:
@@ -168,6 +170,8 @@ def verify(target, draft, tokens, uniforms, T: float, depth=None, need_alpha: bo
     rows = np.arange(B)
     alpha = np.zeros((B, K))
     margin = np.full(B, np.inf)
+    m_acc = np.full(B, np.inf)
+    m_cdf = np.full(B, np.inf)
 
     if T == 0.0:
         g = greedy_argmax(zt)                                   # [B, K+1]
@@ -190,7 +194,8 @@ def verify(target, draft, tokens, uniforms, T: float, depth=None, need_alpha: bo
         with np.errstate(divide="ignore", invalid="ignore"):
             acc_margin = np.where(tested & (qx > 0), np.abs(u[:, :K] - px / qx), np.inf)
         if K > 0:
-            margin = np.minimum(margin, acc_margin.min(axis=1))
+            m_acc = acc_margin.min(axis=1)
+            margin = np.minimum(margin, m_acc)
         rejected = n < d
         # final-draw distribution per request: residual at n if rejected, else p at n (= d)
         p_n = p[rows, n]                                        # [B, V]
@@ -198,15 +203,15 @@ def verify(target, draft, tokens, uniforms, T: float, depth=None, need_alpha: bo
         resid = np.maximum(p_n - q_n, 0.0)
         use_resid = rejected & (np.sum(resid, axis=-1) > 0)     # residual mass 0 only if p == q
         mass = np.where(use_resid[:, None], resid, p_n)
-        final, m = inverse_cdf(mass, u[:, K])
-        margin = np.minimum(margin, m)
+        final, m_cdf = inverse_cdf(mass, u[:, K])
+        margin = np.minimum(margin, m_cdf)
 
     out = np.full((B, K + 1), -1, dtype=np.int64)
     for b in range(B):
         out[b, :n[b]] = x[b, :n[b]]
         out[b, n[b]] = final[b]
     cum, E = cumulative_alpha(alpha)
-    return VerifyResult(out, n.astype(np.int64), alpha, cum, E, margin, d)
+    return VerifyResult(out, n.astype(np.int64), alpha, cum, E, margin, d, m_acc, m_cdf)
 
 
 def overlap_stats(target, draft, T: float):

@@ -44,6 +44,38 @@ def test_hand_example_alpha_and_decisions():
         assert abs(r.expected_len[0] - g["expected_len"]) < 1e-15
 
 
+def test_hand_example_decision_margins():
+    """The two margins the match rule uses, worked by hand for the three cases (derivation in the JSON)."""
+    g = _load("hand_example.json")
+    zt = _logits(g["p"])[None]
+    zd = _logits(g["q"])[None]
+    for case in g["cases"]:
+        r = O.verify(zt, zd, np.array([case["tokens"]]), np.array([case["uniforms"]]), g["T"])
+        assert abs(r.margin_accept[0] - case["margin_accept"]) < 1e-12
+        assert abs(r.margin_cdf[0] - case["margin_cdf"]) < 1e-12
+        assert abs(r.margin[0] - min(case["margin_accept"], case["margin_cdf"])) < 1e-12
+
+
+def test_budget_margin_golden():
+    g = _load("budget_ties.json")
+    a = np.array(g["alpha"])
+    for N, want in g["margin_by_N"].items():
+        assert O.alloc_budget(a, int(N)).margin == want, N
+    assert O.alloc_budget(a, 0).margin == np.inf and O.alloc_budget(a, 9).margin == np.inf
+
+
+def test_greedy_onehot_alpha_golden():
+    """T = 0: alpha is [argmax target == argmax draft], ties in either row going to the lowest index."""
+    g = _load("greedy_onehot_alpha.json")
+    zt = np.array(g["target"], dtype=np.float64)[None]
+    zd = np.array(g["draft"], dtype=np.float64)[None]
+    r = O.verify(zt, zd, np.zeros((1, 2), dtype=int), np.zeros((1, 3)), 0.0)
+    assert r.alpha[0].tolist() == g["alpha"]
+    assert r.cum_alpha[0].tolist() == g["cum_alpha"] and r.expected_len[0] == g["expected_len"]
+    a, c, E = O.overlap_stats(zt, zd, 0.0)
+    assert a[0].tolist() == g["alpha"] and c[0].tolist() == g["cum_alpha"] and E[0] == g["expected_len"]
+
+
 def test_alpha_handbuilt_equals_one_minus_tv():
     for c in _load("alpha_handbuilt.json")["cases"]:
         p, q = np.array(c["p"]), np.array(c["q"])
@@ -394,8 +426,35 @@ def _greedy_pin(mod):
     return r.tokens[0].tolist() == [1, 0]
 
 
+def _margin_pin(mod):
+    g = _load("hand_example.json")
+    ok = True
+    for case in g["cases"]:
+        r = mod.verify(_logits(g["p"])[None], _logits(g["q"])[None], np.array([case["tokens"]]),
+                       np.array([case["uniforms"]]), 1.0)
+        ok &= abs(r.margin_accept[0] - case["margin_accept"]) < 1e-12
+        ok &= abs(r.margin_cdf[0] - case["margin_cdf"]) < 1e-12
+    return bool(ok)
+
+
+def _budget_margin_pin(mod):
+    g = _load("budget_ties.json")
+    a = np.array(g["alpha"])
+    return all(mod.alloc_budget(a, int(N)).margin == m for N, m in g["margin_by_N"].items())
+
+
+def _onehot_pin(mod):
+    g = _load("greedy_onehot_alpha.json")
+    zt = np.array(g["target"], dtype=np.float64)[None]
+    zd = np.array(g["draft"], dtype=np.float64)[None]
+    r = mod.verify(zt, zd, np.zeros((1, 2), dtype=int), np.zeros((1, 3)), 0.0)
+    a, _, _ = mod.overlap_stats(zt, zd, 0.0)
+    return r.alpha[0].tolist() == g["alpha"] and a[0].tolist() == g["alpha"]
+
+
 def test_pins_pass_on_the_real_oracle():
     assert _hist_pin(O) and _hand_pin(O) and _budget_pin(O) and _greedy_pin(O) and _icdf_pin(O)
+    assert _margin_pin(O) and _budget_margin_pin(O) and _onehot_pin(O)
 
 
 @pytest.mark.parametrize("old,new,pin", [
@@ -409,9 +468,24 @@ def test_pins_pass_on_the_real_oracle():
     ("order = np.lexsort((bf, mf, -cf))", "order = np.lexsort((mf, bf, -cf))", "budget"),  # tie order
     ("order = np.lexsort((bf, mf, -cf))", "order = np.lexsort((bf, mf, cf))", "budget"),   # ascending c
     ("return np.argmax(z, axis=-1)", "return z.shape[-1] - 1 - np.argmax(z[..., ::-1], axis=-1)", "greedy"),
+    # decision margins: measured against u * R instead of u, one bin too early, the ratio inverted
+    ("margin = np.minimum(np.abs(Cprev / R - u), np.abs(Cv / R - u))",
+     "margin = np.minimum(np.abs(Cprev - u * R), np.abs(Cv - u * R))", "margin"),
+    ("np.take_along_axis(C, np.maximum(v - 1, 0)[..., None], axis=-1)[..., 0], 0.0)",
+     "np.take_along_axis(C, np.maximum(v - 2, 0)[..., None], axis=-1)[..., 0], 0.0)", "margin"),
+    ("np.abs(u[:, :K] - px / qx)", "np.abs(u[:, :K] - qx / px)", "margin"),
+    # budget margin between the wrong pair of ranked keys
+    ("margin = abs(cf[order[n_sel - 1]] - cf[order[n_sel]])",
+     "margin = abs(cf[order[max(n_sel - 2, 0)]] - cf[order[n_sel - 1]])", "budget_margin"),
+    # T = 0 one-hot alpha comparing the target with itself
+    ("alpha = (g[:, :K] == greedy_argmax(zd)).astype(np.float64)",
+     "alpha = (g[:, :K] == greedy_argmax(zt[:, :K])).astype(np.float64)", "onehot"),
+    ("alpha = (greedy_argmax(zt[:, :K]) == greedy_argmax(zd)).astype(np.float64)",
+     "alpha = (greedy_argmax(zt[:, :K]) == greedy_argmax(zt[:, :K])).astype(np.float64)", "onehot"),
 ])
 def test_pins_catch_planted_mistakes(old, new, pin):
     mod = _mutant(old, new)
     check = {"hist": _hist_pin, "hand": _hand_pin, "budget": _budget_pin, "greedy": _greedy_pin,
-             "icdf": _icdf_pin}[pin]
+             "icdf": _icdf_pin, "margin": _margin_pin, "budget_margin": _budget_margin_pin,
+             "onehot": _onehot_pin}[pin]
     assert not check(mod)
