@@ -1,9 +1,15 @@
 """Benchmark of batched draft verification on GB300.
 
-Default workload: greedy MTP chain verification, B=64 requests, depth K=3,
-V=128000, bf16 target logits [64, 4, 128000], T=0 (argmax matching with the
-bonus token from the target argmax).  One step = one spec_verify_chain call
-(one kernel launch: the row kernel with the fused cut) over one batch.
+Default workload: the batch-level budgeted verification sweep at its largest
+concurrency, B=64 requests, DFly blocks of K=16, V=128000, bf16 logits
+[64, 17, 128000] (target) and [64, 16, 128000] (draft), T=0.9, budget N=8B:
+every position's alpha, the global top-N prefix choice, then verification to
+the chosen depths (540.7 MB of logits per call).  One step = one
+spec_verify_block call (the streaming row kernel, then the budget-and-cut
+kernel chained to it) over one batch.  The verified draft tokens of a step are
+the N positions the budget spends.  The other verification configurations
+(greedy and stochastic MTP chains, DFly block, smaller budget sweeps) are
+measured as secondary lines under "configs".
 
 Timing: W warm-up steps, then exactly K steps replayed from CUDA graphs of
 back-to-back calls, bracketed by a barrier and a device synchronise, timed
@@ -43,9 +49,9 @@ KERNELS = {
     "greedy": {"name": "sv::argmax_kernel<bf16> (argmax + fused cut, one launch)",
                "sources": ["argmax_kernel.cuh", "spec_device.cuh", "spec_internal.h", "budget_cut.cu", "api.cu"],
                "traffic": os.path.join(ROOT, "profiles", "argmax_kernel_traffic.txt")},
-    "sampling": {"name": "sv::sample_kernel<bf16> (+ sv::cut_kernel / budget_cut_kernel, PDL-chained)",
+    "sampling": {"name": "sv::sample_kernel<bf16> (then sv::cut_kernel / sv::budget_cut_kernel, PDL-chained)",
                  "sources": ["sample_kernel.cuh", "spec_async.cuh", "spec_device.cuh", "spec_internal.h", "row_bf16.cu", "api.cu"],
-                 "traffic": os.path.join(ROOT, "profiles", "stream_kernel_traffic.txt")},
+                 "traffic": os.path.join(ROOT, "profiles", "sample_kernel_traffic.txt")},
 }
 
 
@@ -186,6 +192,11 @@ def call_kind(w, name):
     return "block", True
 
 
+def verified_tokens(w) -> int:
+    """Draft positions a step verifies: the budget's N, else every drafted position."""
+    return min(w.budget, w.B * w.K) if w.budget is not None else w.B * w.K
+
+
 def algorithmic_bytes(w, reads_draft: bool) -> int:
     """Bytes the outputs depend on: logits read once + ids/uniforms read + outputs written."""
     e = w.target.element_size()
@@ -261,6 +272,45 @@ class DeviceRunner:
             sv.verify_block(t, d, x, u, w.temperature, budget=w.budget, want_stats=True,
                             stream=self.stream, workspace=self.ws, out=self.out, tuning=tuning)
 
+    def split(self, n=200):
+        """Average device time (us) of the row kernel and of the kernel chained after it, from CUDA
+        events on the launching stream: start, the library's split event between the two launches,
+        stop (the chained kernel then runs without programmatic dependent launch)."""
+        torch = self.torch
+        if self.greedy_fused:
+            return None
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        with torch.cuda.stream(self.stream):
+            for a, m, b in ev:
+                m.record(self.stream)               # creates the event before its handle is passed
+        self.stream.synchronize()
+        with torch.cuda.stream(self.stream):
+            for i, (a, m, b) in enumerate(ev):
+                a.record(self.stream)
+                self.step(i, tuning=self.sv.Tuning(split_event=m))
+                b.record(self.stream)
+        self.stream.synchronize()
+        row = sum(a.elapsed_time(m) for a, m, _ in ev) / n * 1e3
+        cut = sum(m.elapsed_time(b) for _, m, b in ev) / n * 1e3
+        return {"row_kernel_us": row, "chained_kernel_us": cut, "calls": n,
+                "how": "per-call CUDA events around a plain (ungraphed) loop, split event recorded by the "
+                       "library between the two launches"}
+
+    def decisions(self):
+        """One call with every statistic requested: realised mean alpha and accepted length."""
+        torch, sv, w = self.torch, self.sv, self.w
+        t, d, x, u = self.sets[0]
+        with torch.cuda.stream(self.stream):
+            if self.kind == "chain":
+                out = sv.verify_chain(t, w.draft.to(self.dev) if d is None and w.K > 0 else d, x, u, w.temperature,
+                                      want_alpha=True, stream=self.stream, workspace=self.ws)
+            else:
+                out = sv.verify_block(t, d, x, u, w.temperature, budget=w.budget, want_stats=True,
+                                      stream=self.stream, workspace=self.ws)
+        self.stream.synchronize()
+        return out
+
     def launches_per_step(self):
         # greedy without a budget: one argmax kernel with the cut fused in; otherwise the row
         # kernel, then the cut (or budget + cut) kernel chained to it
@@ -334,18 +384,21 @@ def run_gpu(args, rank, local_rank, world):
     clocks = sampler.stop() if sampler else None
     ms_max = max_over_ranks(ms, world, dev)
     per_step_ms = ms_max / args.steps
-    tokens_per_step = w.B * w.K
+    tokens_per_step = verified_tokens(w)
     value = sum_over_ranks(tokens_per_step * args.steps, world, dev) / (ms_max / 1e3)
 
-    # roofline of the (only) kernel of the step: algorithmic bytes / average duration
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else None
     peak_gbs, peak_src = (peaks["hbm_gbs"], "measured") if peaks else (6800.0, "fallback")
-    # the dominant kernel's average duration: with one launch per step it is the step time on
-    # the launching stream; with two, the step time is an upper bound (the chained cut kernel is
-    # a few microseconds and overlaps the row kernel's tail), so `achieved` is a lower bound
-    launch_ms = ms / args.steps
+    step_ms = ms / args.steps
+    # roofline of the dominant kernel: algorithmic bytes / its average duration.  With one launch
+    # per step that is the step time; with two, the row kernel's own time from the split loop.
+    split = r.split() if rank == 0 else None
+    launch_ms = step_ms if split is None else split["row_kernel_us"] / 1e3
     achieved = r.bytes_per_step / (launch_ms / 1e3) / 1e9
+    step_gbs = r.bytes_per_step / (step_ms / 1e3) / 1e9
+    dec_out = r.decisions() if rank == 0 else None
+    decisions = decision_stats(w, dec_out, step_ms / 1e3) if rank == 0 else None
 
     # end to end: pinned host inputs -> device, verify, result -> host, every step
     e2e = run_e2e(w, args, dev, world) if not args.no_e2e else None
@@ -353,6 +406,8 @@ def run_gpu(args, rank, local_rank, world):
     extra = {}
     if rank == 0 and not args.no_extra and world == 1:
         for name in args.extra:
+            if name == args.config:
+                continue
             try:
                 wx = make_workload(name, 0)
                 rx = DeviceRunner(wx, name, dev, min_bytes)
@@ -361,11 +416,19 @@ def run_gpu(args, rank, local_rank, world):
                 msx = rx.run(nsteps)
                 t = msx / nsteps / 1e3
                 bx = rx.bytes_per_step
-                extra[name] = {"tokens_per_s": wx.B * wx.K / t, "rows_per_s": wx.B * (2 * wx.K + 1) / t,
+                sx = rx.split(100)
+                tk = sx["row_kernel_us"] / 1e6 if sx else t
+                extra[name] = {"verified_tokens_per_s": verified_tokens(wx) / t,
+                               "drafted_tokens_per_s": wx.B * wx.K / t,
+                               "rows_per_s": wx.B * (2 * wx.K + 1) / t,
                                "us_per_step": t * 1e6, "logit_bytes": wx.logits_bytes(rx.reads_draft),
-                               "achieved_gbs": bx / t / 1e9, "frac_of_measured_hbm": bx / t / 1e9 / peak_gbs,
-                               "launches_per_step": rx.launches_per_step(), "kernel": KERNELS[rx.kernel_kind]["name"],
-                               "traffic": profiled_traffic(rx.kernel_kind, name)}
+                               "algorithmic_bytes": bx,
+                               "achieved_gbs_step": bx / t / 1e9, "frac_of_measured_hbm_step": bx / t / 1e9 / peak_gbs,
+                               "achieved_gbs_kernel": bx / tk / 1e9, "frac_of_measured_hbm_kernel": bx / tk / 1e9 / peak_gbs,
+                               "split": sx, "launches_per_step": rx.launches_per_step(),
+                               "kernel": KERNELS[rx.kernel_kind]["name"],
+                               "traffic": profiled_traffic(rx.kernel_kind, name),
+                               "decisions": decision_stats(wx, rx.decisions(), t)}
                 del rx
                 torch.cuda.empty_cache()
             except Exception as ex:  # a secondary measurement never hides the main line
@@ -373,7 +436,9 @@ def run_gpu(args, rank, local_rank, world):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        cpu = run_cpu_baseline(w, args.cpu_seconds)
+        cpu = run_cpu_baseline(w, args.cpu_seconds, dec_out)
+        if decisions is not None and cpu is not None:
+            decisions["oracle_agreement"] = cpu.pop("agreement", None)
 
     if rank != 0:
         return None
@@ -383,23 +448,29 @@ def run_gpu(args, rank, local_rank, world):
         "vs_baseline": None, "dtype": "bf16" if w.target.dtype == torch.bfloat16 else "f32",
         "data": "synthetic (seeded; shapes and distributions of the verification configurations)",
         "config": {"workload": f"{args.config} B={w.B} K={w.K} V={w.V} "
-                               f"{'bf16' if w.target.dtype == torch.bfloat16 else 'fp32'} T={w.temperature}",
-                   "B": w.B, "K": w.K, "V": w.V, "temperature": w.temperature, "entry": f"spec_verify_{r.kind}",
-                   "reads_draft": r.reads_draft, "parallelism": f"replicas x{world}",
+                               f"{'bf16' if w.target.dtype == torch.bfloat16 else 'fp32'} T={w.temperature}"
+                               + (f" N={w.budget}" if w.budget is not None else ""),
+                   "B": w.B, "K": w.K, "V": w.V, "temperature": w.temperature, "budget_N": w.budget,
+                   "entry": f"spec_verify_{r.kind}", "reads_draft": r.reads_draft,
+                   "verified_tokens_per_step": tokens_per_step, "parallelism": f"replicas x{world}",
                    "l2": f"inputs rotate over {r.nsets} device copies ({r.nsets * w.logits_bytes(r.reads_draft) / 1e6:.0f} MB > 4x L2 {l2 / 1e6:.0f} MB)",
                    "timing": "CUDA graphs of back-to-back calls, CUDA events on the launching stream",
                    "plan": plan},
-        "rows_per_s": value / max(w.K, 1) * (2 * w.K + 1) if r.reads_draft else value / max(w.K, 1) * (w.K + 1),
-        "achieved_gbs": achieved,
+        "rows_per_s": w.B * (2 * w.K + 1 if r.reads_draft else w.K + 1) / (per_step_ms / 1e3),
+        "achieved_gbs": step_gbs,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_gbs, "unit": "GB/s",
                      "frac": achieved / peak_gbs, "peak_source": f"{peak_src} hbm_gbs (copy, burst)",
                      "traffic": profiled_traffic(r.kernel_kind, args.config),
                      "algorithmic_bytes_per_launch": r.bytes_per_step,
                      "launch_ms": launch_ms, "kernel": KERNELS[r.kernel_kind]["name"],
                      "launches_per_step": r.launches_per_step(),
+                     "step_ms": step_ms, "step_achieved": step_gbs, "step_frac": step_gbs / peak_gbs,
+                     "split": split,
                      "note": ("one launch per step: launch_ms is the step time on the launching stream"
-                              if r.launches_per_step() == 1 else
-                              "two launches per step: launch_ms is the whole step, so achieved is a lower bound")},
+                              if split is None else
+                              "launch_ms is the row kernel's average device time from the split loop; "
+                              "step_* divide by the whole step (row kernel + chained kernel)")},
+        "decisions": decisions,
         "gpu_launches": args.steps * r.launches_per_step(),
         "clocks": clocks,
         "e2e": e2e,
@@ -407,6 +478,22 @@ def run_gpu(args, rank, local_rank, world):
         "configs": extra,
     }
     return line
+
+
+def decision_stats(w, out, step_s):
+    """Realised statistics of one call's decisions (GPU outputs only)."""
+    acc = out.accepted.double().cpu()
+    st = {"mean_accepted": float(acc.mean()), "mean_emitted": float(acc.mean()) + 1.0,
+          "acceptance_rate": float(acc.sum()) / max(1, (int(out.depth.sum()) if out.depth is not None
+                                                        else w.B * w.K)),
+          "accepted_tokens_per_s": float(acc.sum()) / step_s}
+    if out.alpha is not None and w.K > 0:
+        st["mean_alpha"] = float(out.alpha.double().mean())
+    if out.expected_len is not None:
+        st["mean_expected_accepted"] = float(out.expected_len.double().mean())
+    if out.depth is not None:
+        st["mean_depth"] = float(out.depth.double().mean())
+    return st
 
 
 def run_e2e(w, args, dev, world):
@@ -466,36 +553,63 @@ def run_e2e(w, args, dev, world):
 
 # ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
 
-def oracle_step(w, reqs):
+def oracle_pass(w, depth=None, chunk=8):
+    """The float64 oracle over the whole batch (requests in chunks): alpha and the global budget
+    when the workload has one, then the decisions at depth (the budget's, or the one given)."""
     import numpy as np
+    import torch
     from oracle import spec_oracle as O
-    zt = w.target[reqs].to(dtype=__import__("torch").float64).numpy()
-    zd = None if (w.temperature == 0 and w.budget is None) else w.draft[reqs].to(
-        dtype=__import__("torch").float64).numpy()
-    d = None
-    if w.budget is not None:
-        a, _, _ = O.overlap_stats(zt, zd, w.temperature)
-        d = O.alloc_budget(a, max(1, w.budget * len(range(*reqs.indices(w.B))) // w.B)).depth
-    return O.verify(zt, zd, w.tokens[reqs].numpy(), w.uniforms[reqs].double().numpy(), w.temperature,
-                    depth=d, need_alpha=w.temperature > 0)
+    up = lambda t: t.to(dtype=torch.float64).numpy()  # noqa: E731
+    need_draft = not (w.temperature == 0 and w.budget is None)
+    if w.budget is not None and depth is None:
+        a = np.concatenate([O.overlap_stats(up(w.target[s:s + chunk]), up(w.draft[s:s + chunk]), w.temperature)[0]
+                            for s in range(0, w.B, chunk)])
+        depth = O.alloc_budget(a, w.budget).depth
+    parts = []
+    for s in range(0, w.B, chunk):
+        e = min(w.B, s + chunk)
+        parts.append(O.verify(up(w.target[s:e]), up(w.draft[s:e]) if need_draft else None, w.tokens[s:e].numpy(),
+                              w.uniforms[s:e].double().numpy(), w.temperature,
+                              depth=None if depth is None else np.asarray(depth)[s:e],
+                              need_alpha=w.temperature > 0))
+    return parts
 
 
-def run_cpu_baseline(w, seconds: float):
-    """The oracle as it stands, single process, on a bounded sample: whole passes over the batch."""
-    n_req = w.B
+def agreement(w, parts, gpu_out):
+    """Requests whose oracle decision margin is below 1e-5 (ambiguous), and disagreements among the
+    others (bit-exact expected)."""
+    import numpy as np
+    tok = np.concatenate([p.tokens for p in parts])
+    acc = np.concatenate([p.accepted for p in parts])
+    margin = np.concatenate([p.margin for p in parts])
+    g_tok = gpu_out.tokens.cpu().numpy()
+    g_acc = gpu_out.accepted.cpu().numpy()
+    amb = margin < 1e-5
+    differ = (g_acc != acc) | np.any(g_tok != tok, axis=1)
+    return {"requests": int(w.B), "ambiguous": int(amb.sum()), "unambiguous_mismatches": int((differ & ~amb).sum()),
+            "ambiguous_mismatches": int((differ & amb).sum()), "margin_threshold": 1e-5}
+
+
+def run_cpu_baseline(w, seconds: float, gpu_out=None):
+    """The oracle as it stands, single process, on a bounded sample: whole passes over the batch.
+    The first pass runs at the GPU's chosen depths and is compared with the GPU's decisions."""
     t0 = time.perf_counter()
-    passes = 0
-    while True:
-        for s in range(0, w.B, 8):
-            oracle_step(w, slice(s, min(w.B, s + 8)))
+    agree = None
+    if gpu_out is not None:
+        depth = gpu_out.depth.cpu().numpy() if gpu_out.depth is not None else None
+        agree = agreement(w, oracle_pass(w, depth=depth), gpu_out)
+    passes = 1 if gpu_out is not None else 0
+    while passes == 0 or time.perf_counter() - t0 < seconds:
+        oracle_pass(w)
         passes += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
     dt = time.perf_counter() - t0
     cores = _threads_used()
-    return {"value": passes * n_req * w.K / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+    line = {"value": passes * verified_tokens(w) / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{passes} full pass(es) over the {w.B}-request batch in {dt:.1f} s (numpy float64)",
             "cpu": _cpu_model()}
+    if agree is not None:
+        line["agreement"] = agree
+    return line
 
 
 def _threads_used() -> int:
@@ -519,31 +633,40 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     w = make_workload(args.config, 0)
-    # size the per-step sample so the whole run stays within a few minutes
+    # size the per-step sample (whole requests) so the whole run stays within a few minutes
     t0 = time.perf_counter()
-    oracle_step(w, slice(0, 1))
+    oracle_pass(_subset(w, 1))
     per_req = time.perf_counter() - t0
     budget_s = 150.0
     n_req = int(max(1, min(w.B, budget_s / max(1, args.steps + args.warmup) / max(per_req, 1e-6))))
-    for i in range(args.warmup):
-        oracle_step(w, slice(i % w.B, i % w.B + 1))
+    sub = _subset(w, n_req)
+    for _ in range(args.warmup):
+        oracle_pass(_subset(w, 1))
     t0 = time.perf_counter()
-    for i in range(args.steps):
-        s = (i * n_req) % w.B
-        oracle_step(w, slice(s, min(w.B, s + n_req)))
+    for _ in range(args.steps):
+        oracle_pass(sub)
     dt = time.perf_counter() - t0
-    done = sum(min(w.B, (i * n_req) % w.B + n_req) - (i * n_req) % w.B for i in range(args.steps))
-    value = done * w.K / dt
+    value = args.steps * verified_tokens(sub) / dt
     cores = _threads_used()
     return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": f"{args.config} B={w.B} K={w.K} V={w.V} T={w.temperature}"},
+            "config": {"workload": f"{args.config} B={w.B} K={w.K} V={w.V} T={w.temperature}"
+                                   + (f" N={w.budget}" if w.budget is not None else "")},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"{n_req} request(s) of the {w.B}-request batch per step",
+                             "sample": f"{n_req} request(s) of the {w.B}-request batch per step "
+                                       f"(budget scaled to {sub.budget})" if w.budget is not None else
+                                       f"{n_req} request(s) of the {w.B}-request batch per step",
                              "cpu": _cpu_model()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def _subset(w, n):
+    """The first n requests of a workload (the budget scaled with the batch)."""
+    import workloads as W
+    b = None if w.budget is None else max(1, w.budget * n // w.B)
+    return W.Workload(w.name, w.target[:n], w.draft[:n], w.tokens[:n], w.uniforms[:n], w.temperature, b, w.meta)
 
 
 # ---------------------------------------------------------------- main
@@ -554,8 +677,8 @@ def parse(argv=None):
     ap.add_argument("--steps", type=int, default=60000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="greedy_mtp")
-    ap.add_argument("--extra", nargs="*", default=["stochastic_mtp", "dfly_block", "budget_sweep_B4",
+    ap.add_argument("--config", default="budget_sweep_B64")
+    ap.add_argument("--extra", nargs="*", default=["greedy_mtp", "stochastic_mtp", "dfly_block", "budget_sweep_B4",
                                                    "budget_sweep_B16", "budget_sweep_B64"])
     ap.add_argument("--extra-steps", type=int, default=3000)
     ap.add_argument("--no-extra", action="store_true")

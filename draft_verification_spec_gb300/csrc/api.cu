@@ -70,6 +70,7 @@ struct Knobs {
   int cluster = 0;
   int variant = 0;
   int32_t* plan_out = nullptr;
+  cudaEvent_t split = nullptr;
 };
 Knobs knobs_of(const spec_tuning_t* t) {
   Knobs k;
@@ -79,6 +80,7 @@ Knobs knobs_of(const spec_tuning_t* t) {
   k.cluster = t->cluster;
   k.variant = t->greedy_variant & 7;
   k.plan_out = t->plan_out;
+  k.split = static_cast<cudaEvent_t>(t->split_event);
   return k;
 }
 void report_plan(const Knobs& kn, const int (&rec)[8]) {
@@ -476,7 +478,9 @@ spec_status_t run_verify(const VerifyArgs& a, const Knobs& kn) {
   bp.out_E = a.out_E;
   bp.status = status;
   set_sampling_geometry(&bp, plan, mass, a.dtype);
-  const cudaError_t e = budget ? sv::launch_budget_cut(bp, a.stream) : sv::launch_cut(bp, a.depth, a.stream);
+  if (kn.split && cudaEventRecord(kn.split, a.stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  const bool pdl = kn.split == nullptr;
+  const cudaError_t e = budget ? sv::launch_budget_cut(bp, a.stream, pdl) : sv::launch_cut(bp, a.depth, a.stream, pdl);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
@@ -534,7 +538,8 @@ spec_status_t run_overlap(const void* target_logits, const void* draft_logits, i
   bp.out_E = out_expected_len;
   bp.status = status;
   set_sampling_geometry(&bp, plan, mass, dtype);
-  return sv::launch_cut(bp, nullptr, stream) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  if (kn.split && cudaEventRecord(kn.split, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  return sv::launch_cut(bp, nullptr, stream, kn.split == nullptr) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 }  // namespace

@@ -27,7 +27,8 @@ __device__ __forceinline__ float alpha_of(const BudgetParams& P, int b, int k) {
 // One CTA builds the whole confidence table; its warps take requests b = warp, warp + nwarps, ...
 // (grid > 1 only when every CTA can rebuild the table from inputs nobody clears).
 __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid_constant__ BudgetParams P) {
-  extern __shared__ float conf[];   // [B, K] prefix confidences
+  extern __shared__ float conf[];   // [B, K] prefix confidences, then (sampling path) [B, K] alpha
+  float* const alpha_s = conf + P.B * P.K;
   asm volatile("griddepcontrol.wait;" ::: "memory");   // the row kernel's results are complete
   const int B = P.B, K = P.K;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -42,12 +43,12 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid
     }
   } else {
     // sampling path: every row's alpha in parallel (a thread per row), then the prefix products
-    for (int r = threadIdx.x; r < B * K; r += blockDim.x) conf[r] = alpha_of_row(P, r / K, r - (r / K) * K);
+    for (int r = threadIdx.x; r < B * K; r += blockDim.x) alpha_s[r] = alpha_of_row(P, r / K, r - (r / K) * K);
     __syncthreads();
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
       float cp = 1.f;
       for (int k = 0; k < K; ++k) {
-        cp *= conf[b * K + k];
+        cp *= alpha_s[b * K + k];
         conf[b * K + k] = cp;
       }
     }
@@ -84,7 +85,7 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid
         cut_request(b, d, P.stats_only != 0, P.keys, P.draft_keys != 0, false, P.U, K, P.V, P.tokens,
                     P.out_tokens, P.out_accepted, P.out_alpha, P.out_cum, P.out_E, P.status, lane);
       else
-        cut_sampling(P, b, d, lane);
+        cut_sampling(P, b, d, lane, true, lane < K ? alpha_s[b * K + lane] : 0.f);
     }
   }
   if (P.greedy && P.keys) {   // every warp of the (single) CTA is done with the keys: clear them
@@ -111,11 +112,11 @@ __global__ void __launch_bounds__(kCutThreads) cut_kernel(const __grid_constant_
 // Launch chained to the previous kernel on the stream (programmatic dependent launch): the
 // grid may start while the previous one drains and waits for it in griddepcontrol.wait.
 static cudaError_t launch_pdl(const void* fn, int grid, int block, size_t smem, cudaStream_t stream,
-                              void** args) {
+                              void** args, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(block, 1, 1);
   cfg.dynamicSmemBytes = smem;
@@ -125,11 +126,12 @@ static cudaError_t launch_pdl(const void* fn, int grid, int block, size_t smem, 
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-cudaError_t launch_budget_cut(const BudgetParams& p, cudaStream_t stream) {
+cudaError_t launch_budget_cut(const BudgetParams& p, cudaStream_t stream, bool pdl) {
   const int per = kBudgetThreads / 32;
-  // the greedy path clears the keys it reads, so one CTA must own the whole table
+  // the greedy path clears the keys it reads, so one CTA must own the whole table; otherwise every
+  // CTA builds the table and a warp cuts one request
   const int grid = (p.greedy && p.keys) ? 1 : (p.B + per - 1) / per;
-  const size_t smem = static_cast<size_t>(p.B) * p.K * sizeof(float);
+  const size_t smem = static_cast<size_t>(p.B) * p.K * sizeof(float) * ((p.greedy || p.alpha_in) ? 1 : 2);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(budget_cut_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
@@ -138,16 +140,16 @@ cudaError_t launch_budget_cut(const BudgetParams& p, cudaStream_t stream) {
   BudgetParams q = p;
   void* args[] = {&q};
   return launch_pdl(reinterpret_cast<const void*>(&budget_cut_kernel), grid > 0 ? grid : 1, kBudgetThreads,
-                    smem, stream, args);
+                    smem, stream, args, pdl);
 }
 
-cudaError_t launch_cut(const BudgetParams& p, const int32_t* depth, cudaStream_t stream) {
+cudaError_t launch_cut(const BudgetParams& p, const int32_t* depth, cudaStream_t stream, bool pdl) {
   const int per = kCutThreads / 32;
   const int grid = (p.B + per - 1) / per;
   BudgetParams q = p;
   const int32_t* d = depth;
   void* args[] = {&q, &d};
-  return launch_pdl(reinterpret_cast<const void*>(&cut_kernel), grid, kCutThreads, 0, stream, args);
+  return launch_pdl(reinterpret_cast<const void*>(&cut_kernel), grid, kCutThreads, 0, stream, args, pdl);
 }
 
 cudaError_t argmax_blocks_per_sm(bool bf16, int* out) {

@@ -58,13 +58,13 @@ __device__ __forceinline__ float alpha_of_row(const BudgetParams& P, int b, int 
   const float4* a = reinterpret_cast<const float4*>(P.mass + static_cast<size_t>(b * P.U + k) * kMassRowFloats);
   const int nq = P.ncta * 2;                 // float4 per row (8 partials per CTA)
   float s = 0.f;
-  for (int q0 = 0; q0 < nq; q0 += 4) {       // four loads in flight, summed in order
-    float4 v[4];
+  for (int q0 = 0; q0 < nq; q0 += 8) {       // up to eight loads in flight (one round for 4 CTAs)
+    float4 v[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i)
       if (q0 + i < nq) v[i] = __ldcg(a + q0 + i);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i)
       if (q0 + i < nq) s = (((s + v[i].x) + v[i].y) + v[i].z) + v[i].w;
   }
   return fminf(fmaxf(s, 0.f), 1.f);
@@ -74,11 +74,13 @@ __device__ __forceinline__ float alpha_row_warp(const BudgetParams& P, int b, in
   return lane < P.K ? alpha_of_row(P, b, lane) : 0.f;
 }
 
-// The cut of request b at verified depth d (lane k <-> position k).
-__device__ __forceinline__ void cut_sampling(const BudgetParams& P, int b, int d, int lane) {
+// The cut of request b at verified depth d (lane k <-> position k).  alpha_k may be given
+// (alpha_given, lane k's value), as the budget kernel already computed it.
+__device__ __forceinline__ void cut_sampling(const BudgetParams& P, int b, int d, int lane, bool alpha_given = false,
+                                             float alpha_lane = 0.f) {
   const int K = P.K, U = P.U, V = P.V;
   const UnitRec* rb = P.recs + static_cast<size_t>(b) * U;
-  const float a = alpha_row_warp(P, b, lane);
+  const float a = alpha_given ? alpha_lane : alpha_row_warp(P, b, lane);
   write_stats(b, K, a, P.out_alpha, P.out_cum, P.out_E, lane);
   if (P.stats_only) return;
 
@@ -187,17 +189,41 @@ __device__ __forceinline__ void cut_sampling(const BudgetParams& P, int b, int d
     const void* drow = resid ? static_cast<const void*>(static_cast<const uint8_t*>(P.draft) +
                                                         (static_cast<size_t>(b) * K + n) * V * esz)
                              : nullptr;
-    // the draw's mass of segment logit o (piece j of lane l covers [j*PS + l*EPP, +EPP)),
-    // computed exactly as the row kernel did
-    auto mass_at = [&](int o) {
-      if (s0 + o >= nc) return 0.f;
-      const float p = ex2(fmaf(logit_at(trow, v0 + o, P.bf16), P.c, -rn.offt));
-      if (!resid) return p;
-      const float q = ex2(fmaf(logit_at(drow, v0 + o, P.bf16), P.c, -rn.offd));
-      return fmaxf(p - q, 0.f);
-    };
+    // this lane's logits of the segment: piece j covers [j*PS + l*EPP, +EPP) (16 bytes, one vector
+    // load when rows are 16-byte aligned), with the draw's mass computed exactly as the row kernel did
     constexpr int NPC = kSampPieces;
     constexpr int MAXE = 8;                // logits per piece (bf16; fp32 uses the first 4)
+    float zt[NPC][MAXE], zd[NPC][MAXE];
+#pragma unroll
+    for (int j = 0; j < NPC; ++j) {
+      const int o = j * PS + lane * EPP;
+      const bool in = s0 + o < nc;         // whole pieces lie inside or outside the slice when aligned
+      if (P.aligned) {
+        uint4 wt = make_uint4(0, 0, 0, 0), wd = wt;
+        if (in) {
+          wt = __ldcg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(trow) + static_cast<size_t>(v0 + o) * esz));
+          if (resid) wd = __ldcg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(drow) + static_cast<size_t>(v0 + o) * esz));
+        }
+        const uint32_t tw[4] = {wt.x, wt.y, wt.z, wt.w}, dw[4] = {wd.x, wd.y, wd.z, wd.w};
+#pragma unroll
+        for (int e = 0; e < MAXE; ++e) {
+          if (P.bf16) {
+            zt[j][e] = __uint_as_float((e & 1) ? (tw[e >> 1] & 0xffff0000u) : (tw[e >> 1] << 16));
+            zd[j][e] = __uint_as_float((e & 1) ? (dw[e >> 1] & 0xffff0000u) : (dw[e >> 1] << 16));
+          } else {
+            zt[j][e] = __uint_as_float(tw[e & 3]);
+            zd[j][e] = __uint_as_float(dw[e & 3]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < MAXE; ++e) {
+          const bool ok = e < EPP && s0 + o + e < nc;
+          zt[j][e] = ok ? logit_at(trow, v0 + o + e, P.bf16) : 0.f;
+          zd[j][e] = (ok && resid) ? logit_at(drow, v0 + o + e, P.bf16) : 0.f;
+        }
+      }
+    }
     float me[NPC][MAXE];                   // this lane's masses, kept for the element walk
     float sj[NPC], tot[NPC];
 #pragma unroll
@@ -205,8 +231,14 @@ __device__ __forceinline__ void cut_sampling(const BudgetParams& P, int b, int d
       float s = 0.f;
 #pragma unroll
       for (int e = 0; e < MAXE; ++e) {
-        me[j][e] = e < EPP ? mass_at(j * PS + lane * EPP + e) : 0.f;
-        s += me[j][e];
+        const int o = j * PS + lane * EPP + e;
+        float m = 0.f;
+        if (e < EPP && s0 + o < nc) {
+          const float p = ex2(fmaf(zt[j][e], P.c, -rn.offt));
+          m = resid ? fmaxf(p - ex2(fmaf(zd[j][e], P.c, -rn.offd)), 0.f) : p;
+        }
+        me[j][e] = m;
+        s += m;
       }
       sj[j] = s;
       tot[j] = warp_sum(s);

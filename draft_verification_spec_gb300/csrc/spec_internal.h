@@ -143,7 +143,7 @@ struct BudgetParams {
 // Host-side launchers of the small kernels (defined next to them).
 cudaError_t launch_argmax(bool bf16, const ArgmaxParams& p, int grid, cudaStream_t stream);
 cudaError_t argmax_blocks_per_sm(bool bf16, int* out);
-cudaError_t launch_budget_cut(const BudgetParams& p, cudaStream_t stream);
-cudaError_t launch_cut(const BudgetParams& p, const int32_t* depth, cudaStream_t stream);
+cudaError_t launch_budget_cut(const BudgetParams& p, cudaStream_t stream, bool pdl = true);
+cudaError_t launch_cut(const BudgetParams& p, const int32_t* depth, cudaStream_t stream, bool pdl = true);
 
 }  // namespace sv

@@ -7,8 +7,6 @@
 // fixed per model.  For them this entry point keeps its scratch (status word, per-row argmax
 // slots, per-request completion counters) in one file-scope device array of fixed size that
 // every GPU loading the library holds until the process exits.
-#include <mutex>
-
 #include "../../include/spec_verify.h"
 #include "spec_internal.h"
 
@@ -25,22 +23,13 @@ constexpr size_t kStaticBytes = kStatusBytes + kKeysBytes + kCountersBytes;   //
 // device address comes from cudaGetSymbolAddress on each device.
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
-
-// Device address of the scratch on the current device, looked up once per device.
+// Device address of the scratch in the current device's context, looked up on every call (a
+// host-side table lookup once the module is loaded).  Nothing is cached: after a device reset, or
+// in another context on the same device, the module is loaded again and the array can move.
 spec_status_t scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return SPEC_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return SPEC_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return SPEC_ERR_CUDA;
+  *out = p;
   return SPEC_OK;
 }
 

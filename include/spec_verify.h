@@ -188,9 +188,9 @@ spec_status_t spec_alloc_budget(const float* alpha, int B, int K, int budget_N,
  * fixed device array of 80.25 KiB inside the library, held by every GPU that
  * loads it until the process exits:
  * - B * (K + 1) <= SPEC_STATIC_MAX_ROWS (4096), else SPEC_ERR_UNSUPPORTED;
- * - the first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture;
+ * - every call looks up the array's device address in the current device's
+ *   context (cudaGetSymbolAddress); the first call on a device may load the
+ *   module, so make it before any stream capture;
  * - every call clears the parts it uses (cudaMemsetAsync) and shares the one
  *   array, so calls that overlap on the GPU (other streams, other threads)
  *   race: order them on one stream;
@@ -220,6 +220,10 @@ spec_status_t spec_verify_chain_greedy_static(const void* target_logits, const v
  *   greedy_variant  T == 0: bit 1 runs the cut in its own kernel instead of
  *                   fusing it into the argmax kernel; bit 2 launches every
  *                   resident CTA slot with the tiles spread evenly.
+ *   split_event     a cudaEvent_t (as void*) or NULL: recorded on the stream
+ *                   between the row kernel and the kernel chained after it
+ *                   (which is then launched without programmatic dependent
+ *                   launch), so a caller can time the two apart.
  *   plan_out        host int32[8] or NULL: receives the launched plan,
  *                   sampling kernel {threads, cluster, clusters launched, max
  *                   co-resident clusters, slice, ring stages, ring bytes,
@@ -231,6 +235,7 @@ typedef struct spec_tuning {
   int cluster;
   int greedy_variant;
   int32_t* plan_out;
+  void* split_event;
 } spec_tuning_t;
 
 /*

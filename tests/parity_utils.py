@@ -49,6 +49,57 @@ def oracle_alpha(w, chunk=8):
     return np.concatenate(al)
 
 
+# ---------------------------------------------------------------- output guard regions
+CANARY_I32 = 0x7EADBEEF
+CANARY_F32 = -12345.678
+GUARD = 64                       # elements of canary after every output (at least one 128-byte line)
+
+
+def guarded(shape, dtype, device="cuda"):
+    """An output tensor that is a view of a larger buffer whose tail holds a canary.
+
+    Returns (view, buffer); check_guard(buffer, numel) asserts the tail is untouched, catching a
+    kernel that writes past the end of an output (no memory checker runs on these GPUs).
+    """
+    import torch
+    n = 1
+    for d in shape:
+        n *= d
+    fill = CANARY_I32 if dtype == torch.int32 else CANARY_F32
+    buf = torch.full((n + GUARD,), fill, dtype=dtype, device=device)
+    return buf[:n].view(*shape), buf
+
+
+def check_guard(buf, n):
+    import torch
+    tail = buf[n:].cpu()
+    want = CANARY_I32 if buf.dtype == torch.int32 else CANARY_F32
+    assert bool((tail == want).all()), f"output guard overwritten: {tail[:8].tolist()}"
+
+
+def guarded_output(B, K, stats=False, depth=False):
+    """A VerifyOutput whose every tensor has a canary tail, and the list of (buffer, n) to check."""
+    import torch
+    import draft_verification_spec_gb300 as sv
+    parts = []
+
+    def g(shape, dtype):
+        v, b = guarded(shape, dtype)
+        parts.append((b, v.numel()))
+        return v
+    out = sv.VerifyOutput(g((B, K + 1), torch.int32), g((B,), torch.int32),
+                          g((B, K), torch.float32) if stats else None,
+                          g((B, K), torch.float32) if stats else None,
+                          g((B,), torch.float32) if stats else None,
+                          g((B,), torch.int32) if depth else None)
+    return out, parts
+
+
+def check_guards(parts):
+    for b, n in parts:
+        check_guard(b, n)
+
+
 def check_valid_tokens(tokens, accepted, x, V, K):
     B = tokens.shape[0]
     for b in range(B):
@@ -90,6 +141,23 @@ def consistent_within(w, b, tokens_row, n, d, tol=MARGIN):
     C = np.cumsum(mass) / mass.sum()
     lo = C[v - 1] if v > 0 else 0.0
     return lo - tol <= u[K] <= C[v] + tol
+
+
+def check_budget_choice(gdepth, conf_ref, N, margin):
+    """The GPU's depths are a valid budget choice given the float64 prefix confidences.
+
+    Bit-exact against the oracle when its budget margin is >= 1e-5; otherwise several choices are
+    correct, so: sum of depths = min(N, B*K), each depth in [0, K], and every selected key's
+    confidence is at least every dropped key's minus 1e-5 (the selection is a top-N of c).
+    """
+    B, K = conf_ref.shape
+    gdepth = np.asarray(gdepth)
+    assert gdepth.sum() == min(N, B * K)
+    assert np.all((gdepth >= 0) & (gdepth <= K))
+    sel = np.arange(K)[None, :] < gdepth[:, None]
+    if sel.any() and (~sel).any():
+        assert conf_ref[sel].min() >= conf_ref[~sel].max() - MARGIN, (conf_ref[sel].min(), conf_ref[~sel].max())
+    return margin < MARGIN
 
 
 def compare(gpu, ref, w, check_alpha=True):

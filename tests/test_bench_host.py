@@ -54,3 +54,38 @@ def test_profiled_traffic_needs_matching_sources(tmp_path, monkeypatch):
     path.write_text("kernel_source_hash = 0000000000000000\ngreedy_mtp.dram_bytes_per_launch = 123456\n")
     assert bench.profiled_traffic("greedy", "greedy_mtp") is None           # the kernel changed since
 
+
+
+def test_oracle_agreement_counts_a_planted_disagreement():
+    """The bench's decision check: GPU decisions equal the oracle's except where the oracle's margin
+    is below 1e-5; a planted disagreement on an unambiguous request is reported."""
+    import draft_verification_spec_gb300 as sv_mod  # noqa: F401  (only VerifyOutput is used; no GPU)
+    from draft_verification_spec_gb300 import VerifyOutput
+    w = W.random_case(seed=3, B=5, K=3, V=300, T=0.9, dtype=torch.float32)
+    parts = bench.oracle_pass(w)
+    import numpy as np
+    tok = torch.tensor(np.concatenate([p.tokens for p in parts]), dtype=torch.int32)
+    acc = torch.tensor(np.concatenate([p.accepted for p in parts]), dtype=torch.int32)
+    margin = np.concatenate([p.margin for p in parts])
+    out = VerifyOutput(tok.clone(), acc.clone())
+    a = bench.agreement(w, parts, out)
+    assert a["requests"] == 5 and a["unambiguous_mismatches"] == 0 and a["ambiguous_mismatches"] == 0
+    assert a["ambiguous"] == int((margin < 1e-5).sum())
+    b = int(np.argmax(margin))                       # the least ambiguous request
+    out.tokens[b, int(out.accepted[b])] += 1
+    assert bench.agreement(w, parts, out)["unambiguous_mismatches"] == 1
+
+
+def test_reference_arm_budgeted_config_scales_the_budget():
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.main(["--impl", "reference", "--config", "budget_sweep_B4", "--steps", "3", "--warmup", "3"])
+    d = json.loads([ln for ln in buf.getvalue().splitlines() if ln.startswith("{")][0])
+    assert d["impl"] == "reference" and d["value"] > 0
+    assert "N=32" in d["config"]["workload"] and "budget scaled" in d["cpu_baseline"]["sample"]
+
+
+def test_verified_tokens_is_the_budget_when_there_is_one():
+    w = W.budget_sweep(4, V=1000)
+    assert bench.verified_tokens(w) == 32
+    assert bench.verified_tokens(W.greedy_mtp(B=2, V=1000)) == 6
