@@ -143,7 +143,7 @@ class Tuning:
     and the kernel chained after it.  After the call, ``plan`` holds the launched plan.
     """
 
-    KEYS = ("threads", "cluster", "clusters", "max_clusters", "slice", "stages", "ring_bytes", "flags")
+    KEYS = ("threads", "cluster", "clusters", "max_clusters", "slice", "items", "smem_bytes", "flags")
 
     def __init__(self, wait_limit_us: int = 0, cluster: int = 0, greedy_variant: int = 0, split_event=None):
         self._plan = (ctypes.c_int32 * 8)()

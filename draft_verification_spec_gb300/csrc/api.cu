@@ -31,7 +31,6 @@ constexpr int kMaxV = 262144;
 constexpr int kBudgetMaxKeys = 8192;
 constexpr int kSampThreads = 256;
 constexpr int kItemBytes = sv::kSampItemBytes;       // bytes of one row per item of the sampling kernel
-constexpr int kMaxItems = sv::kSampMaxItems;         // items per slice
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -90,10 +89,13 @@ void report_plan(const Knobs& kn, const int (&rec)[8]) {
 // Per-device caches: kernel attributes set once, and occupancy answers.
 std::mutex g_mu;
 std::map<std::tuple<int, const void*>, bool> g_attr_done;
-std::map<std::tuple<int, const void*, int>, int> g_maxc;
+std::map<std::tuple<int, const void*, int, int>, int> g_maxc;
 std::map<int, std::tuple<int, int, size_t>> g_dev;   // SMs, L2 bytes
-// chosen sampling plan (cluster size, clusters launched, resident clusters) per call shape
-std::map<std::tuple<int, const void*, int, int, int, int, int>, std::tuple<int, int, int>> g_plans;
+// chosen sampling plan per call shape
+struct PlanChoice {
+  int cluster, nclusters, maxc;
+};
+std::map<std::tuple<int, const void*, int, int, int, int, int>, PlanChoice> g_plans;
 
 cudaError_t device_info(int dev, int* sms, size_t* l2) {
   {
@@ -117,11 +119,11 @@ cudaError_t device_info(int dev, int* sms, size_t* l2) {
   return cudaSuccess;
 }
 
-cudaError_t prepare_kernel(int dev, const void* fn) {
+cudaError_t prepare_kernel(int dev, const void* fn, int smem_max) {
   std::lock_guard<std::mutex> lk(g_mu);
   auto key = std::make_tuple(dev, fn);
   if (g_attr_done.count(key)) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, sv::kSampRingBytes);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
@@ -129,17 +131,18 @@ cudaError_t prepare_kernel(int dev, const void* fn) {
   return cudaSuccess;
 }
 
-// Largest number of clusters of `cluster` sampling CTAs that can be resident at once.
-cudaError_t max_clusters(int dev, const void* fn, int cluster, int* out) {
+// Largest number of clusters of `cluster` sampling CTAs, each with `smem` bytes of dynamic shared
+// memory, that can be resident at once.
+cudaError_t max_clusters(int dev, const void* fn, int smem_max, int cluster, int smem, int* out) {
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    auto it = g_maxc.find(std::make_tuple(dev, fn, cluster));
+    auto it = g_maxc.find(std::make_tuple(dev, fn, cluster, smem));
     if (it != g_maxc.end()) {
       *out = it->second;
       return cudaSuccess;
     }
   }
-  cudaError_t e = prepare_kernel(dev, fn);
+  cudaError_t e = prepare_kernel(dev, fn, smem_max);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -149,36 +152,34 @@ cudaError_t max_clusters(int dev, const void* fn, int cluster, int* out) {
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(cluster, 1, 1);
   cfg.blockDim = dim3(kSampThreads, 1, 1);
-  cfg.dynamicSmemBytes = sv::kSampRingBytes;
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
   e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lk(g_mu);
-  g_maxc[std::make_tuple(dev, fn, cluster)] = n;
+  g_maxc[std::make_tuple(dev, fn, cluster, smem)] = n;
   *out = n;
   return cudaSuccess;
 }
 
 struct RowPlan {
   const void* fn;
-  int cluster, nclusters, maxc;
+  int cluster, nclusters, maxc, smem;
   RowParams p;
 };
 
 // Estimated duration (seconds) of the sampling kernel with clusters of C CTAs: units go
-// round-robin to the clusters (pairs first); a CTA streams its slice of a unit's rows at its
-// share of the HBM bandwidth (pass 2 overlaps the next unit's pass 1), and every step pays a
-// fixed cost for the cluster exchange and the normalisers.  The constants were fitted to timings
-// of the verification configurations on a GB300 (effective 3 TB/s shared by the CTAs, at most
-// 15 GB/s per CTA, 2 us per step).
-double plan_cost(int C, int ncl, int npairs, int nsingle, double row_bytes) {
+// round-robin to the clusters (pairs first); a CTA reads its slice of a unit's rows at its share
+// of the HBM bandwidth (bw_total over all CTAs, at most bw_cta each) and every step pays a fixed
+// cost t_step for the cluster exchange and the normalisers.
+double plan_cost(int C, int ncl, int npairs, int nsingle, double row_bytes, double bw_total, double bw_cta,
+                 double t_step) {
   const int units = npairs + nsingle;
   if (ncl < 1) return 1e300;
-  const double bw = std::fmin(3.0e12 / (static_cast<double>(ncl) * C), 1.5e10);
+  const double bw = std::fmin(bw_total / (static_cast<double>(ncl) * C), bw_cta);
   const double t_row = row_bytes / C / bw;
-  const double t_step = 2.0e-6;
   double worst = 0.0;
   for (int j = 0; j < ncl && j < units; ++j) {
     double t = t_step;
@@ -187,6 +188,8 @@ double plan_cost(int C, int ncl, int npairs, int nsingle, double row_bytes) {
   }
   return worst;
 }
+// Fitted to timings of the verification configurations on a GB300.
+constexpr double kPlanBw = 6.5e12, kPlanBwCta = 2.5e10, kPlanStep = 1.5e-6;
 
 spec_status_t plan_rows(const void* target, const void* draft, int dtype, int B, int K, int V, float T,
                         bool need_draft, bool stats_only, const Knobs& kn, RowPlan* plan) {
@@ -197,63 +200,49 @@ spec_status_t plan_rows(const void* target, const void* draft, int dtype, int B,
   const void* fn = bf16 ? sv::sample_kernel_bf16(aligned) : sv::sample_kernel_f32(aligned);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
-  int sms = 0;
-  size_t l2 = 0;
-  if (device_info(dev, &sms, &l2) != cudaSuccess) return SPEC_ERR_CUDA;
   const int npairs = need_draft ? B * K : 0;
   const int nsingle = stats_only ? 0 : (need_draft ? B : B * (K + 1));
   const int units = npairs + nsingle;
   const double row_bytes = static_cast<double>(V) * esz;
-  // a slice holds at most kMaxItems items of 8 KB per row
-  const long long min_c = (static_cast<long long>(V) * esz + static_cast<long long>(kMaxItems) * kItemBytes - 1) /
-                          (static_cast<long long>(kMaxItems) * kItemBytes);
-  int best_c = 0, best_ncl = 0, best_maxc = 0;
+  const int item_logits = kItemBytes / esz;
+  auto slice_of = [&](int C) { return static_cast<int>(align_up((V + C - 1) / C, sv::kChunk)); };
+  auto items_of = [&](int C) { return (slice_of(C) + item_logits - 1) / item_logits; };
+  PlanChoice best = {0, 0, 0};
   const auto key = std::make_tuple(dev, fn, B, K, V, static_cast<int>(need_draft) | (stats_only ? 2 : 0), kn.cluster);
   {
     std::lock_guard<std::mutex> lk(g_mu);
     auto it = g_plans.find(key);
-    if (it != g_plans.end()) std::tie(best_c, best_ncl, best_maxc) = it->second;
+    if (it != g_plans.end()) best = it->second;
   }
-  if (best_c == 0) {
-    // the bytes streamed between a logit's first and second read must fit in the L2 with room to
-    // spare, or the second pass goes back to HBM; among the sizes that keep it there, the cheapest
-    // estimated schedule wins (the largest size if none does)
-    bool best_fits = false;
-    double best = 1e300;
+  if (best.cluster == 0) {
+    // among the cluster sizes whose slice fits the slab, the cheapest estimated schedule
+    double best_cost = 1e300;
     for (int C = 1; C <= sv::kMaxCluster; C *= 2) {
-      if (C < min_c) continue;
       if (kn.cluster && C != kn.cluster) continue;
+      const int itmax = items_of(C);
+      if (itmax > sv::kSampMaxItems || C * itmax > sv::kMassMaxSegments) continue;
       int maxc = 0;
-      if (max_clusters(dev, fn, C, &maxc) != cudaSuccess) return SPEC_ERR_CUDA;
+      if (max_clusters(dev, fn, sv::kSampMaxSlabBytes, C, sv::samp_slab_bytes(itmax), &maxc) != cudaSuccess)
+        return SPEC_ERR_CUDA;
       if (maxc < 1) continue;
       const int ncl = units < maxc ? units : maxc;
-      const double window = static_cast<double>(ncl) * (need_draft ? 2.0 : 1.0) * row_bytes;
-      const bool fits = kn.cluster != 0 || window <= 0.75 * static_cast<double>(l2);
-      const double cost = plan_cost(C, ncl, npairs, nsingle, row_bytes);
-      const bool better = (fits && !best_fits) || (fits == best_fits && (fits ? cost < best * 0.97 : C > best_c));
-      if (best_c == 0 || better) {
-        best = cost;
-        best_fits = fits;
-        best_c = C;
-        best_ncl = ncl;
-        best_maxc = maxc;
+      const double cost = plan_cost(C, ncl, npairs, nsingle, row_bytes, kPlanBw, kPlanBwCta, kPlanStep);
+      if (best.cluster == 0 || cost < best_cost * 0.97) {
+        best_cost = cost;
+        best = {C, ncl, maxc};
       }
     }
-    if (best_c == 0) return SPEC_ERR_UNSUPPORTED;
+    if (best.cluster == 0) return SPEC_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lk(g_mu);
-    g_plans[key] = std::make_tuple(best_c, best_ncl, best_maxc);
+    g_plans[key] = best;
   }
-  if (best_c == 0) return SPEC_ERR_UNSUPPORTED;
-  int slice = (V + best_c - 1) / best_c;
-  slice = static_cast<int>(align_up(slice, sv::kChunk));
-  if (static_cast<long long>(slice) * esz > static_cast<long long>(kMaxItems) * kItemBytes) return SPEC_ERR_UNSUPPORTED;
-  const int item_logits = kItemBytes / esz;
-  const int itmax = (slice + item_logits - 1) / item_logits;
-  if (best_c * itmax > sv::kMassMaxSegments) return SPEC_ERR_UNSUPPORTED;
+  const int slice = slice_of(best.cluster);
+  const int itmax = items_of(best.cluster);
   plan->fn = fn;
-  plan->cluster = best_c;
-  plan->nclusters = best_ncl;
-  plan->maxc = best_maxc;
+  plan->cluster = best.cluster;
+  plan->nclusters = best.nclusters;
+  plan->maxc = best.maxc;
+  plan->smem = sv::samp_slab_bytes(itmax);
   RowParams& p = plan->p;
   std::memset(&p, 0, sizeof(p));
   p.target = target;
@@ -275,7 +264,7 @@ spec_status_t plan_rows(const void* target, const void* draft, int dtype, int B,
 spec_status_t launch_plan(RowPlan* plan, const Knobs& kn, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
-  if (prepare_kernel(dev, plan->fn) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (prepare_kernel(dev, plan->fn, sv::kSampMaxSlabBytes) != cudaSuccess) return SPEC_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -288,14 +277,14 @@ spec_status_t launch_plan(RowPlan* plan, const Knobs& kn, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(plan->nclusters * plan->cluster, 1, 1);
   cfg.blockDim = dim3(kSampThreads, 1, 1);
-  cfg.dynamicSmemBytes = sv::kSampRingBytes;
+  cfg.dynamicSmemBytes = static_cast<size_t>(plan->smem);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   void* args[] = {&plan->p};
   if (cudaLaunchKernelExC(&cfg, plan->fn, args) != cudaSuccess) return SPEC_ERR_CUDA;
   const int rec[8] = {kSampThreads, plan->cluster, plan->nclusters, plan->maxc, plan->p.slice,
-                      sv::kSampStages, sv::kSampRingBytes, plan->p.flags};
+                      plan->p.itmax, plan->smem, plan->p.flags};
   report_plan(kn, rec);
   return SPEC_OK;
 }

@@ -1,4 +1,4 @@
-// fp32 instantiations of the sampling row kernel (16-byte aligned rows, and any rows).
+// f32 instantiations of the sampling row kernel (16-byte aligned rows, and any rows).
 #include "sample_kernel.cuh"
 
 namespace sv {

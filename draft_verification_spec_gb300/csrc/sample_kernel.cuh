@@ -1,32 +1,28 @@
-// Sampling-path row kernel (T > 0): two streaming passes per (request, position) unit,
-// software-pipelined across units.
+// Sampling-path row kernel (T > 0): two passes per (request, position) unit over a CTA's slice of
+// the unit's rows, which stays in shared memory between them, so HBM is read once.
 //
 // A thread-block cluster of C CTAs works on a sequence of units -- target row k and, for k < K,
 // draft row k -- (persistent; units go round-robin to clusters, pairs first).  CTA r owns the
-// vocabulary slice [r*slice, (r+1)*slice) of every row and walks it in items of kSampItemBytes per
-// row; warp w owns bytes [w*kSampWarpBytes, (w+1)*kSampWarpBytes) of every item.  Every lane
-// streams its own kSampPieces 16-byte pieces of each row with asynchronous copies (cp.async, L2
-// only) into its own slots of the warp's ring of kSampStages stages in shared memory,
-// kSampStages - 1 items ahead across steps, one commit group per item: the bytes in flight cost
-// no registers and a wait is one cp.async.wait_group, no polling.  (Rows that do not start on
-// 16-byte boundaries are read element-wise from global memory instead.)
-//
-// Step s of a CTA walks the items of two units at once: pass 1 of unit s (from HBM) and pass 2 of
-// unit s - 1 (the same bytes it read one step earlier, now L2 hits), so the HBM stream never
-// pauses for a second pass.
-//   pass 1: per-lane online (max, sum of 2^((z - m) c)) of the target and draft rows -> warp
-//     maximum and rescaled warp sum -> exchange #1 with st.async into every CTA of the cluster,
-//     completing on its mbarrier -> the row normalisers of p and q, merged in one fixed order so
-//     every warp of every CTA holds bitwise-identical values; p_k(x_k), q_k(x_k) and the accept
-//     test, exactly as the cut kernel evaluates them afterwards
-//   pass 2: per logit p = 2^(z c - offt), q = 2^(z c - offd).  A pair that passes the test and
-//     needs no draw only needs alpha = sum 2^min(a, b) (one exp2 per logit pair); otherwise every
-//     warp writes its (item, warp) masses of r = max(0, p - q) and of p to the row's mass table.
-//     Every warp writes its alpha partial.  No second exchange: the chained cut kernel sums the
-//     partials in one fixed order and makes the single draw each request needs (at its first
-//     rejection, or the bonus) from the mass table, reloading only that one segment.
-// A target row that no draw needs is skipped entirely.  DRAM reads each needed logit once while
-// the bytes streamed between a logit's two reads fit in L2.
+// vocabulary slice [r*slice, (r+1)*slice) of every row and holds its bytes of the current unit in
+// a shared-memory slab of itmax items of kSampItemBytes per row.  Warp w owns bytes
+// [w*kSampWarpBytes, (w+1)*kSampWarpBytes) of every item and each lane its kSampPieces 16-byte
+// pieces of those, so the lane that copies a piece is the only one that ever reads it: no barrier
+// sits between a copy and its use, and a wait is one cp.async.wait_group.
+//   pass 1, as the unit's asynchronous copies land (one commit group per item): per-lane online
+//     (max, sum of 2^((z - m) c)) of the target and draft rows -> warp maximum and rescaled warp
+//     sum -> exchange with st.async into every CTA of the cluster, completing on its mbarrier ->
+//     the row normalisers of p and q, merged in one fixed order so every warp of every CTA holds
+//     bitwise-identical values; p_k(x_k), q_k(x_k) and the accept test, exactly as the cut kernel
+//     evaluates them afterwards
+//   pass 2, from shared memory: per logit p = 2^(z c - offt), q = 2^(z c - offd).  A pair that
+//     passes the test and needs no draw only needs alpha = sum 2^min(a, b) (one exp2 per logit
+//     pair); otherwise every warp writes its (item, warp) masses of r = max(0, p - q) and of p to
+//     the row's mass table.  Every warp writes its alpha partial.  As soon as a lane is done with
+//     an item, it copies its pieces of the next unit's item into the same bytes.
+// The draws themselves are made by the chained cut kernel from the mass tables.  While a CTA
+// waits on its cluster's exchange, the other CTAs resident on its SM keep HBM busy.  A target row
+// that no draw needs is skipped entirely.  Rows that do not start on 16-byte boundaries are read
+// element-wise in pass 1 and stored to the slab for pass 2.
 //
 // Every wait is bounded by wall time.  A wait that runs out records SPEC_ERR_DEVICE_TIMEOUT and
 // then waits once more with a long limit, so the exchange protocol stays consistent and no peer
@@ -34,6 +30,8 @@
 // does the CTA stop waiting (abort mode; results unspecified).  Every phase a CTA arms it also
 // waits for, so on the normal path no peer store can arrive after the CTA has exited.
 #pragma once
+
+#include <type_traits>
 
 #include <cuda_bf16.h>
 
@@ -110,72 +108,62 @@ __device__ __forceinline__ float words_max(const uint32_t (&w)[N]) {
   }
 }
 
-// 16 read-only bytes from global memory, not kept in L1 (each byte is used once per pass).
-__device__ __forceinline__ void ldg16(uint32_t* w, const uint8_t* p) {
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-               : "l"(p));
+// 16-byte asynchronous copy global -> shared by this thread (cached in L2 only, evict-first: every
+// byte is read from global memory once).  The form without a source-size operand: a piece is
+// either copied whole or not at all.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const uint8_t* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
+               : "memory");
 }
-
-// 16-byte asynchronous copy global -> shared by this thread (cached in L2 only).
-__device__ __forceinline__ void cp_async16(uint32_t dst, const uint8_t* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-// First entry (vocabulary order: lane-major, EPL entries per lane) whose running prefix
-// cum0 + sum(..) crosses t; if rounding leaves none, the last entry with positive mass; -1 if
-// none has mass.  Uniform across the warp.  *cum_before = cum0 + mass before the chosen entry.
-template <int EPL>
-__device__ __forceinline__ int select_entry(const float (&m)[EPL], float cum0, float t, int lane,
-                                            float* cum_before) {
-  float loc = 0.f;
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) loc += m[i];
-  const float incl = warp_incl_scan(loc, lane);
-  float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-  if (lane == 0) excl = 0.f;
-  int first = -1, lastpos = -1;
-  float run = cum0 + excl, before = 0.f, lb = 0.f;
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    if (first < 0 && run + m[i] > t) { first = i; before = run; }
-    if (m[i] > 0.f) { lastpos = i; lb = run; }
-    run += m[i];
+// wait_group with a run-time depth (uniform across the CTA); deeper than 15 waits for everything
+__device__ __forceinline__ void cp_async_wait_upto(int n) {
+  switch (n) {
+    case 15: cp_async_wait<15>(); break;
+    case 14: cp_async_wait<14>(); break;
+    case 13: cp_async_wait<13>(); break;
+    case 12: cp_async_wait<12>(); break;
+    case 11: cp_async_wait<11>(); break;
+    case 10: cp_async_wait<10>(); break;
+    case 9: cp_async_wait<9>(); break;
+    case 8: cp_async_wait<8>(); break;
+    case 7: cp_async_wait<7>(); break;
+    case 6: cp_async_wait<6>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 1: cp_async_wait<1>(); break;
+    default: cp_async_wait<0>(); break;
   }
-  const unsigned hit = __ballot_sync(0xffffffffu, first >= 0);
-  int sel = -1;
-  float cb = cum0;
-  if (hit) {
-    const int l = __ffs(hit) - 1;
-    sel = l * EPL + __shfl_sync(0xffffffffu, first, l);
-    cb = __shfl_sync(0xffffffffu, before, l);
-  } else {
-    const unsigned pos = __ballot_sync(0xffffffffu, lastpos >= 0);
-    if (pos) {
-      const int l = 31 - __clz(pos);
-      sel = l * EPL + __shfl_sync(0xffffffffu, lastpos, l);
-      cb = __shfl_sync(0xffffffffu, lb, l);
-    }
-  }
-  *cum_before = cb;
-  return sel;
 }
 
-// Pass-2 work of a unit.
-enum : int { M2_ALPHA = 0, M2_FULL = 1, M2_SINGLE = 2 };
+__device__ __forceinline__ void lds16(uint32_t* w, uint32_t addr) {
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void sts16(uint32_t addr, const uint32_t* w) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+               : "memory");
+}
 
-// A unit as a CTA walks it: its row slices, its record, its exchange buffers.
+// A unit as a CTA walks it: its row slices, its record, its exchange slot.
 struct SampUnit {
   const uint8_t* gt;       // target row slice (this CTA's part)
   const uint8_t* gd;       // draft row slice (pairs)
   int b, k, rec, idx;      // request, position, record index, needed-unit ordinal of this CTA
   bool pair, pdraw;
-  int x;                   // drafted token (lane 0; prefetched when the unit is taken)
-  float uk;                // its accept uniform (prefetched)
-  float ztx, zdx;          // target and draft logits at x (lane 0; loaded during pass 1)
+  int x;                   // drafted token (lane 0)
+  float uk;                // its accept uniform
+  float ztx, zdx;          // target and draft logits at x (lane 0)
 };
 
 template <bool BF16, bool ALIGNED>
@@ -184,16 +172,14 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
   constexpr int ESZ = G::ESZ, EPP = G::EPP, NPC = G::NPC, NWD = G::NWD;
   constexpr int IL = G::IL, WS = G::WS, PS = G::PS;
   constexpr int NWARP = kSampWarps;
-  constexpr int IB = kSampItemBytes;
-  constexpr int ENT = kMaxCluster * NWARP;         // exchange #1 entries per row: (CTA c, warp w) at c*NWARP + w
+  constexpr int IB = kSampItemBytes, WB = kSampWarpBytes;
+  constexpr int ENT = kMaxCluster * NWARP;         // exchange entries per row: (CTA c, warp w) at c*NWARP + w
   constexpr int EPL = ENT / 32;
   constexpr int NQ = BF16 ? NWD : NWD / 2;         // logit pairs per lane per row per item
   constexpr uint32_t NEG = BF16 ? 0xff80ff80u : 0xff800000u;
 
-  constexpr int S = kSampStages, WB = kSampWarpBytes;
-  // warp w's ring: stage s, row slot r (0: pass-1 target, 1: pass-1 draft, 2: pass-2 target,
-  // 3: pass-2 draft) at byte ((w * S + s) * 4 + r) * WB
-  extern __shared__ __align__(128) uint8_t ring[];
+  // the slab: warp w, item it, row r (0 target, 1 draft) at byte ((w * itmax + it) * 2 + r) * WB
+  extern __shared__ __align__(128) uint8_t slab[];
   __shared__ __align__(16) float4 mbox1[2][ENT];               // (m_t, s_t, m_d, s_d) per (CTA, warp)
   __shared__ __align__(8) uint64_t x1_bar[2];
   __shared__ int abort_flag;
@@ -202,6 +188,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
   const uint32_t rank = cluster_rank(), C = cluster_ncta();
   const uint32_t cid = cluster_idx(), ncl = cluster_count();
   const int K = P.K, V = P.V;
+  const int itmax = P.itmax;
   const int lo = static_cast<int>(rank) * P.slice;
   const int n = max(0, min(P.slice, V - lo));                  // this CTA's slice length
   const int nitems = (n + IL - 1) / IL;
@@ -214,9 +201,14 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
                          ? (P.total_units - static_cast<int>(cid) + static_cast<int>(ncl) - 1) / static_cast<int>(ncl)
                          : 0;
   const int npairs = need_draft ? P.B * K : 0;   // units [0, npairs) are (target, draft) pairs
-  // this lane's byte offset of piece j of item it: it * IB + wl + j * 512; its first logit: + el
-  const int wl = warp * kSampWarpBytes + lane * 16;
+  // this lane's byte offset of piece j of item it in a row slice: it * IB + wl + j * 512; its
+  // first logit there: it * IL + el + j * PS
+  const int wl = warp * WB + lane * 16;
   const int el = warp * WS + lane * EPP;
+  // logits of this warp's part of the last item that lie inside the slice
+  const int last_nval = nitems > 0 ? min(WS, max(0, n - (nitems - 1) * IL - warp * WS)) : 0;
+  const uint32_t slab_l = smem_addr(slab) + static_cast<uint32_t>(warp * itmax * 2 * WB + lane * 16);
+  auto slot = [&](int it, int r) -> uint32_t { return slab_l + static_cast<uint32_t>((it * 2 + r) * WB); };
 
   // unit u -> (b, k): the pairs first (b-major), then the target rows k = K (or, without draft
   // rows, every target row); larger units first gives round-robin assignment a short tail
@@ -248,6 +240,16 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
     abort_flag = 0;
   }
   mbar_fence_init();
+  // pieces of the last item past the slice end are never copied: they hold -inf for good
+  if (nitems > 0) {
+    const uint32_t neg[4] = {NEG, NEG, NEG, NEG};
+#pragma unroll
+    for (int j = 0; j < NPC; ++j)
+      if (j * PS + lane * EPP >= last_nval) {
+        sts16(slot(nitems - 1, 0) + j * 512, neg);
+        sts16(slot(nitems - 1, 1) + j * 512, neg);
+      }
+  }
   __syncthreads();
   cluster_sync();   // every CTA's barriers exist before any peer sends into them
   // launched with programmatic serialization: the logits, tokens and records are touched only
@@ -255,9 +257,10 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const long long wlimit = P.wait_limit;
-  // A bounded wait on an exchange phase (completed by peers' stores; acquire at cluster scope).
-  // On timeout record it, then wait with the long limit; if that also runs out, switch the CTA to
-  // abort mode (no more waiting).  The common case reads no clock.
+  // A bounded wait on an exchange phase (completed by peers' stores; acquire at cluster scope), by
+  // one thread while the rest of the CTA waits at a barrier without issuing.  On timeout record
+  // it, then wait with the long limit; if that also runs out, switch the CTA to abort mode (no
+  // more waiting).  The common case reads no clock.
   auto wait_phase = [&](uint32_t bar, uint32_t parity) {
     if (wlimit > 0 && mbar_try_cluster(bar, parity)) return true;
     if (*static_cast<volatile int*>(&abort_flag)) return mbar_try_cluster(bar, parity);
@@ -268,34 +271,49 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
     return false;
   };
 
-  // this lane's words of item `it` of a row (slice base g): NPC 16-byte pieces, -inf past the
-  // slice end (only the last item can reach it)
-  auto row_words = [&](uint32_t (&W)[NWD], const uint8_t* g, int it, bool last) {
+  // rows not on 16-byte boundaries: this lane's words of item `it` of a row (slice base g),
+  // element by element, -inf past the slice end
+  auto row_words = [&](uint32_t (&W)[NWD], const uint8_t* g, int it) {
 #pragma unroll
     for (int j = 0; j < NPC; ++j) {
-      if constexpr (ALIGNED) {
-        if (!last || it * IL + el + j * PS < n) {
-          ldg16(&W[4 * j], g + static_cast<size_t>(it) * IB + wl + j * 512);
-        } else {
+      const int o = it * IL + el + j * PS;       // first logit of the piece in the slice
 #pragma unroll
-          for (int q = 0; q < 4; ++q) W[4 * j + q] = NEG;
-        }
-      } else {
-        const int o = it * IL + el + j * PS;     // first logit of the piece in the slice
+      for (int q = 0; q < 4; ++q) W[4 * j + q] = NEG;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) W[4 * j + q] = NEG;
-#pragma unroll
-        for (int e = 0; e < EPP; ++e) {
-          if (o + e < n) {
-            if constexpr (BF16) {
-              const uint32_t h16 = reinterpret_cast<const uint16_t*>(g)[o + e];
-              uint32_t& w = W[4 * j + (e >> 1)];
-              w = (e & 1) ? ((w & 0x0000ffffu) | (h16 << 16)) : ((w & 0xffff0000u) | h16);
-            } else {
-              W[4 * j + e] = reinterpret_cast<const uint32_t*>(g)[o + e];
-            }
+      for (int e = 0; e < EPP; ++e) {
+        if (o + e < n) {
+          if constexpr (BF16) {
+            const uint32_t h16 = reinterpret_cast<const uint16_t*>(g)[o + e];
+            uint32_t& w = W[4 * j + (e >> 1)];
+            w = (e & 1) ? ((w & 0x0000ffffu) | (h16 << 16)) : ((w & 0xffff0000u) | h16);
+          } else {
+            W[4 * j + e] = reinterpret_cast<const uint32_t*>(g)[o + e];
           }
         }
+      }
+    }
+  };
+  auto slab_words = [&](uint32_t (&W)[NWD], uint32_t addr) {
+#pragma unroll
+    for (int j = 0; j < NPC; ++j) lds16(&W[4 * j], addr + j * 512);
+  };
+  auto slab_store = [&](uint32_t addr, const uint32_t (&W)[NWD]) {
+#pragma unroll
+    for (int j = 0; j < NPC; ++j) sts16(addr + j * 512, &W[4 * j]);
+  };
+
+  // one item of a unit into the slab (t, d: this lane's first byte of the row slices; d null for
+  // a target row alone)
+  const uint64_t policy = l2_evict_first_policy();
+  auto issue_item = [&](const uint8_t* t, const uint8_t* d, int it) {
+    const size_t off = static_cast<size_t>(it) * IB;
+    const uint32_t dst = slot(it, 0);
+    const bool full = it != nitems - 1;
+#pragma unroll
+    for (int j = 0; j < NPC; ++j) {
+      if (full || j * PS + lane * EPP < last_nval) {
+        cp_async16(dst + j * 512, t + off + j * 512, policy);
+        if (d) cp_async16(dst + WB + j * 512, d + off + j * 512, policy);
       }
     }
   };
@@ -324,115 +342,16 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
   };
 
   // ---------------------------------------------------------------- the unit sequence
-  // A: in pass 1 during the current step.  B: in pass 2 during the current step.
-  // The next needed unit at or after cursor `cur` (advanced past it), if any.
-  auto next_needed = [&](int& cur, int& b, int& k, bool& pair, bool& pdraw) -> bool {
-    for (; cur < nunits; ++cur) {
-      unit_of(cur, b, k);
-      pair = need_draft && k < K;
-      pdraw = pdraw_row(b, k);
-      if (pair || pdraw) {
-        ++cur;
-        return true;
-      }
-    }
-    return false;
-  };
-  auto row_slice = [&](bool draft, int b, int k) {
-    return draft ? static_cast<const uint8_t*>(P.draft) + ((static_cast<size_t>(b) * K + k) * static_cast<size_t>(V) + lo) * ESZ
-                 : static_cast<const uint8_t*>(P.target) + ((static_cast<size_t>(b) * (K + 1) + k) * static_cast<size_t>(V) + lo) * ESZ;
-  };
-
-  // ---- this lane's copy ring, S - 1 items ahead of the consumer, across steps
-  const uint32_t ring_w = smem_addr(ring) + static_cast<uint32_t>(warp * S * 4 * WB) + static_cast<uint32_t>(lane) * 16u;
-  const int last_nval = nitems > 0 ? min(WS, max(0, n - (nitems - 1) * IL - warp * WS)) : 0;
-  int icur = 0, iit = 0, istage = 0;
-  bool ihA = false, ihB = false, iApair = false, iBpair = false;
-  const uint8_t *iAt = nullptr, *iAd = nullptr, *iBt = nullptr, *iBd = nullptr;
-  auto issue_take = [&]() {
-    int b, k;
-    bool pair, pdraw;
-    ihA = next_needed(icur, b, k, pair, pdraw);
-    if (ihA) {
-      iApair = pair;
-      iAt = row_slice(false, b, k) + wl;
-      iAd = pair ? row_slice(true, b, k) + wl : iAt;
-    }
-  };
-  if (ALIGNED && nitems > 0) issue_take();
-  // every step of the sequence commits one group (possibly empty), so wait_group(S - 1)
-  // always retires exactly the oldest item
-  auto issue_next = [&]() {
-    if (ihA || ihB) {
-      const size_t off = static_cast<size_t>(iit) * IB;
-      const uint32_t dst = ring_w + static_cast<uint32_t>(istage * 4 * WB);
-      const bool full = iit != nitems - 1;
-#pragma unroll
-      for (int j = 0; j < NPC; ++j) {
-        if (full || static_cast<int>(j * PS + lane * EPP) < last_nval) {
-          if (ihA) {
-            cp_async16(dst + j * 512, iAt + off + j * 512);
-            if (iApair) cp_async16(dst + WB + j * 512, iAd + off + j * 512);
-          }
-          if (ihB) {
-            cp_async16(dst + 2 * WB + j * 512, iBt + off + j * 512);
-            if (iBpair) cp_async16(dst + 3 * WB + j * 512, iBd + off + j * 512);
-          }
-        }
-      }
-    }
-    cp_async_commit();
-    if (!(ihA || ihB)) return;
-    istage = istage == S - 1 ? 0 : istage + 1;
-    if (++iit == nitems) {                          // the next step: A moves to pass 2
-      iit = 0;
-      ihB = ihA;
-      iBpair = iApair;
-      iBt = iAt;
-      iBd = iAd;
-      issue_take();
-    }
-  };
-  for (int q = 0; q < S - 1; ++q) issue_next();
-  int cstage = 0;
-  // the next item's stage: issue the one S - 1 further on (into the stage this lane finished
-  // with last step), retire this one; returns this lane's address of row slot 0
-  auto acquire = [&]() -> uint32_t {
-    issue_next();
-    cp_async_wait<S - 1>();
-    const uint32_t base = ring_w + static_cast<uint32_t>(cstage * 4 * WB);
-    cstage = cstage == S - 1 ? 0 : cstage + 1;
-    return base;
-  };
-  // this lane's words of one row slot of the stage; -inf past the slice end on the last item
-  auto slot_words = [&](uint32_t (&W)[NWD], uint32_t addr, bool last) {
-#pragma unroll
-    for (int j = 0; j < NPC; ++j) {
-      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(W[4 * j]), "=r"(W[4 * j + 1]), "=r"(W[4 * j + 2]), "=r"(W[4 * j + 3])
-                   : "r"(addr + j * 512));
-      if (last) {
-#pragma unroll
-        for (int e = 0; e < EPP; ++e) {
-          if (j * PS + lane * EPP + e >= last_nval) {
-            if constexpr (BF16) {
-              uint32_t& w = W[4 * j + (e >> 1)];
-              w = (e & 1) ? ((w & 0x0000ffffu) | 0xff800000u) : ((w & 0xffff0000u) | 0x0000ff80u);
-            } else {
-              W[4 * j + e] = NEG;
-            }
-          }
-        }
-      }
-    }
-  };
-
   int iu = 0;                                // next unit index to look at
   int taken = 0;                             // needed units taken so far
   auto take_unit = [&](SampUnit& U) -> bool {   // the next needed unit, if any
-    int b, k;
-    bool pair, pdraw;
-    if (next_needed(iu, b, k, pair, pdraw)) {
+    for (; iu < nunits; ++iu) {
+      int b, k;
+      unit_of(iu, b, k);
+      const bool pair = need_draft && k < K;
+      const bool pdraw = pdraw_row(b, k);
+      if (!(pair || pdraw)) continue;
+      ++iu;
       U.b = b;
       U.k = k;
       U.rec = b * P.U + k;
@@ -444,7 +363,6 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
       U.gd = pair ? static_cast<const uint8_t*>(P.draft) +
                         ((static_cast<size_t>(b) * K + k) * static_cast<size_t>(V) + lo) * ESZ
                   : U.gt;
-      // the accept test's operands, fetched a step before they are needed
       const bool tested = !stats_only && k < K;
       U.x = (tested && lane == 0) ? __ldg(&P.tokens[static_cast<size_t>(b) * K + k]) : -1;
       U.uk = tested ? __ldg(&P.uniforms[static_cast<size_t>(b) * (K + 1) + k]) : 0.f;
@@ -453,7 +371,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
     }
     return false;
   };
-  // lane 0: the logits at the drafted token (issued once the token has had time to arrive)
+  // lane 0: the logits at the drafted token
   auto fetch_at_token = [&](SampUnit& U) {
     if (lane == 0 && U.x >= 0 && U.x < V) {
       const size_t ot = (static_cast<size_t>(U.b) * (K + 1) + U.k) * V + U.x;
@@ -468,188 +386,199 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
     }
   };
 
-  SampUnit A = {}, B = {};
-  bool hasA = take_unit(A), hasB = false;
-  if (hasA && tid == 0) mbar_arrive_tx(smem_addr(&x1_bar[A.idx & 1]), static_cast<uint32_t>(nent) * 16u);
-  // B's pass-2 parameters (set when it leaves pass 1)
-  int modeB = kModeAlpha;
-  float offtB = 0.f, offdB = 0.f;
-  const int itmax = P.itmax;
-
-  while (hasA || hasB) {
-    // ---- the items of this step: pass 1 of A (HBM), pass 2 of B (L2)
-    float mt = ninf(), st = 0.f, md = ninf(), sd = 0.f;
-    uint64_t aacc = pk(0.f, 0.f), bacc = aacc;     // B in alpha mode
-    float pw = 0.f, rw = 0.f;                      // B in full mode: the warp's totals (lanes 16 / 0)
-    const uint64_t noff_t = pk(-offtB, -offtB), noff_d = pk(-offdB, -offdB);
-    const uint64_t neg1 = pk(-1.f, -1.f);
-    float* const mB = P.mass + static_cast<size_t>(B.rec) * kMassRowFloats;
+  // pass 1 of a unit over the slab; PAIR: the draft row too
+  auto pass1 = [&](auto pair_tag, const SampUnit& A, float& mt, float& st, float& md, float& sd) {
+    constexpr bool PAIR = decltype(pair_tag)::value;
     for (int it = 0; it < nitems; ++it) {
-      const bool last = it == nitems - 1;
-      uint32_t At[NWD], Ad[NWD], Bt[NWD], Bd[NWD];
-      // every load of the step's item first, then the arithmetic
+      uint32_t Wt[NWD], Wd[NWD];
       if constexpr (ALIGNED) {
-        const uint32_t base = acquire();
-        const bool rag = last && last_nval < WS;
-        if (hasA) {
-          slot_words(At, base, rag);
-          if (A.pair) slot_words(Ad, base + WB, rag);
+        cp_async_wait_upto(nitems - 1 - it);        // this lane's pieces of the item have landed
+        slab_words(Wt, slot(it, 0));
+        if constexpr (PAIR) slab_words(Wd, slot(it, 1));
+      } else {
+        row_words(Wt, A.gt, it);
+        slab_store(slot(it, 0), Wt);
+        if constexpr (PAIR) {
+          row_words(Wd, A.gd, it);
+          slab_store(slot(it, 1), Wd);
         }
-        if (hasB) {
-          slot_words(Bt, base + 2 * WB, rag);
-          if (modeB != kModeSingle) slot_words(Bd, base + 3 * WB, rag);
+      }
+      fold(Wt, mt, st);
+      if constexpr (PAIR) fold(Wd, md, sd);
+    }
+  };
+
+  // pass 2 of a unit from the slab; each item, once consumed, takes the next unit's copies
+  // (nT / nD: this lane's first byte of its row slices, nT null if there is none).  MODE: alpha
+  // only, full masses, or target masses alone.  Returns the warp's alpha partial (lane-uniform).
+  auto pass2 = [&](auto mode_tag, float offt, float offd, float* mrow, const uint8_t* nT, const uint8_t* nD) -> float {
+    constexpr int MODE = decltype(mode_tag)::value;
+    const uint64_t noff_t = pk(-offt, -offt), noff_d = pk(-offd, -offd);
+    const uint64_t neg1 = pk(-1.f, -1.f);
+    uint64_t aacc = pk(0.f, 0.f), bacc = aacc;
+    float pw = 0.f, rw = 0.f;                      // full / single: the warp's totals (lanes 16 / 0)
+    for (int it = 0; it < nitems; ++it) {
+      uint32_t Wt[NWD], Wd[NWD];
+      slab_words(Wt, slot(it, 0));
+      if constexpr (MODE != kModeSingle) slab_words(Wd, slot(it, 1));
+      if constexpr (MODE == kModeAlpha) {
+#pragma unroll
+        for (int q = 0; q < NQ; q += 2) {
+          float a0, a1, b0, b1, a2, a3, b2, b3;
+          upk(ffma2(pair_of<BF16>(Wt, q), c2, noff_t), a0, a1);
+          upk(ffma2(pair_of<BF16>(Wd, q), c2, noff_d), b0, b1);
+          upk(ffma2(pair_of<BF16>(Wt, q + 1), c2, noff_t), a2, a3);
+          upk(ffma2(pair_of<BF16>(Wd, q + 1), c2, noff_d), b2, b3);
+          aacc = fadd2(aacc, pk(ex2(fminf(a0, b0)), ex2(fminf(a1, b1))));
+          bacc = fadd2(bacc, pk(ex2(fminf(a2, b2)), ex2(fminf(a3, b3))));
         }
       } else {
-        if (hasA) {
-          row_words(At, A.gt, it, last);
-          if (A.pair) row_words(Ad, A.gd, it, last);
+        uint64_t pacc = pk(0.f, 0.f), racc = pacc;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          float a0, a1;
+          upk(ffma2(pair_of<BF16>(Wt, q), c2, noff_t), a0, a1);
+          const uint64_t p = pk(ex2(a0), ex2(a1));     // p of logits 2q, 2q+1
+          pacc = fadd2(pacc, p);
+          if constexpr (MODE == kModeFull) {
+            float b0, b1, d0, d1;
+            upk(ffma2(pair_of<BF16>(Wd, q), c2, noff_d), b0, b1);
+            upk(ffma2(pk(ex2(b0), ex2(b1)), neg1, p), d0, d1);   // p - q
+            racc = fadd2(racc, pk(fmaxf(d0, 0.f), fmaxf(d1, 0.f)));
+          }
         }
-        if (hasB) {
-          row_words(Bt, B.gt, it, last);
-          if (modeB != kModeSingle) row_words(Bd, B.gd, it, last);
-        }
-      }
-      if (hasB) {
-        if (modeB == kModeAlpha) {
+        float p0, p1, r0, r1;
+        upk(pacc, p0, p1);
+        upk(racc, r0, r1);
+        // lanes 0-15 end with the warp's R, lanes 16-31 with its P (one exchange of each at 16)
+        const bool hi = (lane & 16) != 0;
+        float keep = hi ? p0 + p1 : r0 + r1;
+        keep += __shfl_xor_sync(0xffffffffu, hi ? r0 + r1 : p0 + p1, 16);
 #pragma unroll
-          for (int q = 0; q < NQ; q += 2) {
-            float a0, a1, b0, b1, a2, a3, b2, b3;
-            upk(ffma2(pair_of<BF16>(Bt, q), c2, noff_t), a0, a1);
-            upk(ffma2(pair_of<BF16>(Bd, q), c2, noff_d), b0, b1);
-            upk(ffma2(pair_of<BF16>(Bt, q + 1), c2, noff_t), a2, a3);
-            upk(ffma2(pair_of<BF16>(Bd, q + 1), c2, noff_d), b2, b3);
-            aacc = fadd2(aacc, pk(ex2(fminf(a0, b0)), ex2(fminf(a1, b1))));
-            bacc = fadd2(bacc, pk(ex2(fminf(a2, b2)), ex2(fminf(a3, b3))));
-          }
-        } else {
-          uint64_t pacc = pk(0.f, 0.f), racc = pacc;
-          if (modeB == kModeFull) {
-#pragma unroll
-            for (int q = 0; q < NQ; ++q) {
-              float a0, a1, b0, b1, d0, d1;
-              upk(ffma2(pair_of<BF16>(Bt, q), c2, noff_t), a0, a1);
-              const uint64_t p = pk(ex2(a0), ex2(a1));     // p of logits 2q, 2q+1
-              pacc = fadd2(pacc, p);
-              upk(ffma2(pair_of<BF16>(Bd, q), c2, noff_d), b0, b1);
-              upk(ffma2(pk(ex2(b0), ex2(b1)), neg1, p), d0, d1);   // p - q
-              racc = fadd2(racc, pk(fmaxf(d0, 0.f), fmaxf(d1, 0.f)));
-            }
-          } else {
-#pragma unroll
-            for (int q = 0; q < NQ; ++q) {
-              float a0, a1;
-              upk(ffma2(pair_of<BF16>(Bt, q), c2, noff_t), a0, a1);
-              pacc = fadd2(pacc, pk(ex2(a0), ex2(a1)));
-            }
-          }
-          float p0, p1, r0, r1;
-          upk(pacc, p0, p1);
-          upk(racc, r0, r1);
-          // lanes 0-15 end with the warp's R, lanes 16-31 with its P (one exchange of each at 16)
-          const bool hi = (lane & 16) != 0;
-          float keep = hi ? p0 + p1 : r0 + r1;
-          keep += __shfl_xor_sync(0xffffffffu, hi ? r0 + r1 : p0 + p1, 16);
-#pragma unroll
-          for (int o = 8; o; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
-          if ((lane & 15) == 0) {
-            mB[kMassAlphaFloats + ((static_cast<int>(rank) * itmax + it) * NWARP + warp) * 2 + (lane >> 4)] = keep;
-            if (hi) pw += keep; else rw += keep;
-          }
+        for (int o = 8; o; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
+        if ((lane & 15) == 0) {
+          mrow[kMassAlphaFloats + ((static_cast<int>(rank) * itmax + it) * NWARP + warp) * 2 + (lane >> 4)] = keep;
+          if (hi) pw += keep; else rw += keep;
         }
       }
-      if (hasA) {
-        fold(At, mt, st);
-        if (A.pair) fold(Ad, md, sd);
-        if (it == 0) fetch_at_token(A);
+      if constexpr (ALIGNED) {
+        // the item's words are in registers and used: the next unit's copies take its bytes
+        if (nT) issue_item(nT, nD, it);
+        cp_async_commit();
       }
     }
+    if constexpr (MODE == kModeAlpha) {
+      float a0, a1;
+      upk(fadd2(aacc, bacc), a0, a1);
+      return warp_sum(a0 + a1);
+    } else {
+      // sum p - R over this warp's items (lane 16 holds P, lane 0 holds R)
+      return __shfl_sync(0xffffffffu, pw, 16) - __shfl_sync(0xffffffffu, rw, 0);
+    }
+  };
 
-    // ---- A: warp partials (warp maximum, then every lane's sum rescaled to it) -> exchange #1
-    if (hasA) {
+  SampUnit A = {};
+  bool hasA = take_unit(A);
+  if constexpr (ALIGNED) {
+    // the first unit's slice, one commit group per item; pass 2 commits one group per item too,
+    // so when pass 1 consumes item it, the groups after it are items it+1 .. nitems-1
+    if (hasA)
+      for (int it = 0; it < nitems; ++it) {
+        issue_item(A.gt + wl, A.pair ? A.gd + wl : nullptr, it);
+        cp_async_commit();
+      }
+  }
+
+  while (hasA) {
+    const int apar = A.idx & 1;
+    if (tid == 0) mbar_arrive_tx(smem_addr(&x1_bar[apar]), static_cast<uint32_t>(nent) * 16u);
+    fetch_at_token(A);
+
+    // ---- pass 1, then the warp partials (warp maximum, every lane's sum rescaled to it) to every
+    // CTA of the cluster
+    float mt = ninf(), st = 0.f, md = ninf(), sd = 0.f;
+    if (A.pair) pass1(std::true_type(), A, mt, st, md, sd);
+    else pass1(std::false_type(), A, mt, st, md, sd);
+    {
       const float wt = warp_max(mt), wd = warp_max(md);
       const float rt = wt == ninf() ? 0.f : wt, rd = wd == ninf() ? 0.f : wd;
       st = warp_sum(st * ex2((mt - rt) * c));
       sd = warp_sum(sd * ex2((md - rd) * c));
       if (lane < static_cast<int>(C)) {
-        const uint32_t dst = smem_addr(&mbox1[A.idx & 1][rank * NWARP + warp]);
-        st_async_v4(peer_addr(dst, lane), wt, st, wd, sd, peer_addr(smem_addr(&x1_bar[A.idx & 1]), lane));
+        const uint32_t dst = smem_addr(&mbox1[apar][rank * NWARP + warp]);
+        st_async_v4(peer_addr(dst, lane), wt, st, wd, sd, peer_addr(smem_addr(&x1_bar[apar]), lane));
       }
     }
 
-    // ---- B: this warp's alpha partial into the row's mass table
-    if (hasB) {
-      float aw;
-      if (modeB == kModeAlpha) {
-        float a0, a1;
-        upk(fadd2(aacc, bacc), a0, a1);
-        aw = warp_sum(a0 + a1);
-      } else {
-        // sum p - R over this warp's items (lane 16 holds P, lane 0 holds R)
-        aw = __shfl_sync(0xffffffffu, pw, 16) - __shfl_sync(0xffffffffu, rw, 0);
+    // ---- the row normalisers and the accept test (the barrier carries thread 0's acquire of the
+    // peers' partials to the whole CTA)
+    if (tid == 0) wait_phase(smem_addr(&x1_bar[apar]), (A.idx >> 1) & 1);
+    __syncthreads();
+    float Mt = ninf(), Md = ninf();
+#pragma unroll
+    for (int q = 0; q < EPL; ++q) {
+      const int e = lane * EPL + q;
+      if (e < nent) {
+        const float4 v = mbox1[apar][e];
+        Mt = fmaxf(Mt, v.x);
+        Md = fmaxf(Md, v.z);
       }
-      if (lane == 0) mB[static_cast<int>(rank) * NWARP + warp] = aw;
     }
-
-    // ---- A leaves pass 1: normalisers and the accept test; it becomes B, the next unit A
-    hasB = hasA;
-    if (hasA) {
-      const int apar = A.idx & 1;
-      wait_phase(smem_addr(&x1_bar[apar]), (A.idx >> 1) & 1);
-      float Mt = ninf(), Md = ninf();
+    Mt = warp_max(Mt);
+    Md = warp_max(Md);
+    float St = 0.f, Sd = 0.f;
+    {
+      const float rt = (Mt == ninf()) ? 0.f : Mt, rd = (Md == ninf()) ? 0.f : Md;
 #pragma unroll
       for (int q = 0; q < EPL; ++q) {
         const int e = lane * EPL + q;
         if (e < nent) {
           const float4 v = mbox1[apar][e];
-          Mt = fmaxf(Mt, v.x);
-          Md = fmaxf(Md, v.z);
+          St += v.y * ex2((v.x - rt) * c);
+          Sd += v.w * ex2((v.z - rd) * c);
         }
       }
-      Mt = warp_max(Mt);
-      Md = warp_max(Md);
-      float St = 0.f, Sd = 0.f;
-      {
-        const float rt = (Mt == ninf()) ? 0.f : Mt, rd = (Md == ninf()) ? 0.f : Md;
-#pragma unroll
-        for (int q = 0; q < EPL; ++q) {
-          const int e = lane * EPL + q;
-          if (e < nent) {
-            const float4 v = mbox1[apar][e];
-            St += v.y * ex2((v.x - rt) * c);
-            Sd += v.w * ex2((v.z - rd) * c);
-          }
-        }
-      }
-      St = warp_sum(St);
-      Sd = warp_sum(Sd);
-      // p_v = 2^(z c - offt), q_v = 2^(z c - offd): the normalisers folded into the exponent
-      offtB = (Mt == ninf() ? 0.f : Mt * c) + lg2f(St);
-      offdB = (Md == ninf() ? 0.f : Md * c) + lg2f(Sd);
-      float px = 0.f, qx = 0.f;
-      const bool xin = lane == 0 && A.x >= 0 && A.x < V;
-      if (xin) {
-        px = ex2(fmaf(A.ztx, c, -offtB));
-        qx = ex2(fmaf(A.zdx, c, -offdB));
-      }
-      px = __shfl_sync(0xffffffffu, px, 0);
-      qx = __shfl_sync(0xffffffffu, qx, 0);
-      const bool xin_all = __shfl_sync(0xffffffffu, xin ? 1 : 0, 0) != 0;
-      const bool rejects = !stats_only && A.k < K && !(xin_all && A.uk * qx < px);
-      // a pair that passes the test and draws nothing needs only alpha = sum min(p, q), and
-      // min(2^a, 2^b) = 2^min(a, b): one exp2 per logit pair and no mass table
-      modeB = A.pair ? ((!rejects && !A.pdraw) ? kModeAlpha : kModeFull) : kModeSingle;
-      if (rank == 0 && tid == 0) {
-        UnitRec* r = P.recs + A.rec;
-        r->px = px;
-        r->qx = qx;
-        r->offt = offtB;
-        r->offd = offdB;
-        r->mode = modeB;
-      }
-      B = A;
-      hasA = take_unit(A);
-      if (hasA && tid == 0) mbar_arrive_tx(smem_addr(&x1_bar[A.idx & 1]), static_cast<uint32_t>(nent) * 16u);
     }
+    St = warp_sum(St);
+    Sd = warp_sum(Sd);
+    // p_v = 2^(z c - offt), q_v = 2^(z c - offd): the normalisers folded into the exponent
+    const float offt = (Mt == ninf() ? 0.f : Mt * c) + lg2f(St);
+    const float offd = (Md == ninf() ? 0.f : Md * c) + lg2f(Sd);
+    float px = 0.f, qx = 0.f;
+    const bool xin = lane == 0 && A.x >= 0 && A.x < V;
+    if (xin) {
+      px = ex2(fmaf(A.ztx, c, -offt));
+      qx = ex2(fmaf(A.zdx, c, -offd));
+    }
+    px = __shfl_sync(0xffffffffu, px, 0);
+    qx = __shfl_sync(0xffffffffu, qx, 0);
+    const bool xin_all = __shfl_sync(0xffffffffu, xin ? 1 : 0, 0) != 0;
+    const bool rejects = !stats_only && A.k < K && !(xin_all && A.uk * qx < px);
+    // a pair that passes the test and draws nothing needs only alpha = sum min(p, q), and
+    // min(2^a, 2^b) = 2^min(a, b): one exp2 per logit pair and no mass table
+    const int mode = A.pair ? ((!rejects && !A.pdraw) ? kModeAlpha : kModeFull) : kModeSingle;
+    if (rank == 0 && tid == 0) {
+      UnitRec* r = P.recs + A.rec;
+      r->px = px;
+      r->qx = qx;
+      r->offt = offt;
+      r->offd = offd;
+      r->mode = mode;
+    }
+
+    // ---- pass 2, handing the slab over to the next unit item by item
+    SampUnit N = {};
+    const bool hasN = take_unit(N);
+    const uint8_t* nT = hasN ? N.gt + wl : nullptr;
+    const uint8_t* nD = (hasN && N.pair) ? N.gd + wl : nullptr;
+    float* const mrow = P.mass + static_cast<size_t>(A.rec) * kMassRowFloats;
+    float aw;
+    if (mode == kModeAlpha) aw = pass2(std::integral_constant<int, kModeAlpha>(), offt, offd, mrow, nT, nD);
+    else if (mode == kModeFull) aw = pass2(std::integral_constant<int, kModeFull>(), offt, offd, mrow, nT, nD);
+    else aw = pass2(std::integral_constant<int, kModeSingle>(), offt, offd, mrow, nT, nD);
+    if (lane == 0) mrow[static_cast<int>(rank) * NWARP + warp] = aw;
+    A = N;
+    hasA = hasN;
   }
   cp_async_wait<0>();                        // only empty groups remain; retire them before leaving
 }

@@ -16,21 +16,18 @@ constexpr int kMaxK = 31;         // drafted positions per request (lanes 0..K o
 #define SPEC_SAMP_PIECES 2
 #endif
 #ifndef SPEC_SAMP_MINB
-#define SPEC_SAMP_MINB 2
-#endif
-#ifndef SPEC_SAMP_STAGES
-#define SPEC_SAMP_STAGES 3
+#define SPEC_SAMP_MINB 3
 #endif
 constexpr int kSampWarps = 8;
 constexpr int kSampPieces = SPEC_SAMP_PIECES;
 constexpr int kSampWarpBytes = kSampPieces * 512;                    // one row, one item, one warp
 constexpr int kSampItemBytes = kSampWarps * kSampWarpBytes;           // one row, one item
-constexpr int kSampMaxItems = 32;                                     // items per slice
 constexpr int kSampMinBlocks = SPEC_SAMP_MINB;                        // resident CTAs per SM the registers allow
-// Aligned rows are staged through each warp's ring of kSampStages stages, a stage holding the
-// warp's bytes of one item of four rows (pass-1 target, draft; pass-2 target, draft).
-constexpr int kSampStages = SPEC_SAMP_STAGES;
-constexpr int kSampRingBytes = kSampWarps * kSampStages * 4 * kSampWarpBytes;   // dynamic shared memory
+// A CTA's slice of a unit (target and draft row) stays in a shared-memory slab of at most
+// kSampMaxItems items per row between the two passes.
+constexpr int kSampMaxItems = 12;
+constexpr int samp_slab_bytes(int items) { return kSampWarps * items * 2 * kSampWarpBytes; }
+constexpr int kSampMaxSlabBytes = samp_slab_bytes(kSampMaxItems);
 
 // Status bits in the workspace's device status word.
 constexpr int kStatusTimeout = 1;
@@ -86,7 +83,7 @@ struct ArgmaxParams {
 enum : int {
   F_NEED_DRAFT = 1,   // draft rows are read for positions k < K
   F_STATS_ONLY = 2,   // rows k < K only; alpha, no draws
-  F_ALIGNED = 8,      // rows start on 16-byte boundaries: staged by 1-D bulk copies
+  F_ALIGNED = 8,      // rows start on 16-byte boundaries: staged by 16-byte asynchronous copies
   F_ALL_PDRAWS = 16,  // draw from p at every row (the verified depth is chosen afterwards)
 };
 

@@ -215,8 +215,8 @@ spec_status_t spec_verify_chain_greedy_static(const void* target_logits, const v
  *                   then waits once more, up to 100 ms, so its copies and
  *                   cluster exchanges still complete before it returns).
  *   cluster         T > 0: CTAs per row of the sampling kernel (1, 2, 4, 8 or
- *                   16; a slice must not exceed 32 items of 8 KB per row, else
- *                   SPEC_ERR_UNSUPPORTED); 0: chosen per call shape.
+ *                   16; a CTA's slice must not exceed 12 items of 8 KB per
+ *                   row, else SPEC_ERR_UNSUPPORTED); 0: chosen per call shape.
  *   greedy_variant  T == 0: bit 1 runs the cut in its own kernel instead of
  *                   fusing it into the argmax kernel; bit 2 launches every
  *                   resident CTA slot with the tiles spread evenly.
@@ -226,9 +226,10 @@ spec_status_t spec_verify_chain_greedy_static(const void* target_logits, const v
  *                   launch), so a caller can time the two apart.
  *   plan_out        host int32[8] or NULL: receives the launched plan,
  *                   sampling kernel {threads, cluster, clusters launched, max
- *                   co-resident clusters, slice, ring stages, ring bytes,
- *                   flags}; argmax kernel {threads, 1, grid, resident CTAs,
- *                   tile, 0, 0, -1}.
+ *                   co-resident clusters, slice, items per slice, dynamic
+ *                   shared memory bytes, flags};
+ *                   argmax kernel {threads, 1, grid, resident CTAs, tile, 0,
+ *                   0, -1}.
  */
 typedef struct spec_tuning {
   long long wait_limit_us;

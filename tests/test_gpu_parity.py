@@ -5,6 +5,8 @@ the benchmark times; small and ragged shapes cover the tails (unaligned rows,
 partial chunks, empty CTA slices, a single vocabulary entry) and the
 degenerate cases of the method (K = 0, alpha = 1, disjoint supports, ties).
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -115,13 +117,13 @@ CASES = [
     (3, 2, 2, 0.7, torch.float32),
     (2, 3, 17, 1.0, torch.bfloat16),       # unaligned rows: element-wise path
     (3, 5, 1000, 0.9, torch.float32),
-    (2, 4, 1004, 1.3, torch.float32),      # fp32 bulk copy with a half chunk at the tail
+    (2, 4, 1004, 1.3, torch.float32),      # fp32 16-byte copies; the last item is mostly past the row end
     (3, 3, 1023, 0.9, torch.bfloat16),     # unaligned bf16
     (2, 2, 8191, 0.0, torch.bfloat16),
     (2, 7, 8200, 0.5, torch.bfloat16),     # two CTAs per row, ragged second slice
     (1, 31, 3000, 1.0, torch.float32),     # K at its limit
     (2, 3, 40000, 0.9, torch.bfloat16),
-    (2, 2, 131080, 0.9, torch.bfloat16),   # 512-thread CTAs
+    (2, 2, 131080, 0.9, torch.bfloat16),   # above 128K: a ragged item in every CTA slice
     (1, 2, 262144, 1.1, torch.bfloat16),   # largest V
     (1, 1, 262144, 0.0, torch.float32),
 ]
@@ -390,7 +392,7 @@ def test_fp32_block_with_budget(sv):
 
 # ---------------------------------------------------------------- fp32 rows split over several CTAs
 
-@pytest.mark.parametrize("V,cluster", [(65536, 0), (65536, 2), (131072, 0), (131072, 4)])
+@pytest.mark.parametrize("V,cluster", [(65536, 0), (65536, 4), (131072, 0), (131072, 8)])
 def test_fp32_multi_cta_chain_block_budget(sv, V, cluster):
     """fp32 logits at T > 0 with the row split over a cluster (the DSMEM exchange of fp32 partials)."""
     w = W.random_case(seed=31 + V // 1024 + cluster, B=3, K=3, V=V, T=0.9, dtype=torch.float32)
@@ -412,11 +414,57 @@ def test_fp32_multi_cta_chain_block_budget(sv, V, cluster):
     assert sv.default_workspace().status() == 0
 
 
+def _slab_fits(V, esz, cluster):
+    """Whether a CTA slice fits the sampling kernel's shared-memory slab (12 items of 8 KB per row,
+    at most 80 (CTA, item) segments per row)."""
+    slice_ = math.ceil(math.ceil(V / cluster) / 8) * 8
+    items = math.ceil(slice_ * esz / 8192)
+    return items <= 12 and cluster * items <= 80
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("V,cluster", [(24, 16), (4104, 1), (4099, 2), (50008, 4), (128000, 4), (128000, 8),
+                                       (128000, 16)])
+def test_slab_sizes(sv, dtype, V, cluster):
+    """Every slab size the planner can pick gives the oracle's results: chain, block with a budget,
+    and alpha alone (empty CTA slices at V = 24 over 16 CTAs, unaligned rows at V = 4099, ragged
+    last items elsewhere); a forced cluster size whose slice does not fit is refused."""
+    esz = 2 if dtype == torch.bfloat16 else 4
+    w = W.random_case(seed=V + cluster + esz, B=3, K=4, V=V, T=0.9, dtype=dtype)
+    if not _slab_fits(V, esz, cluster):
+        with pytest.raises(sv.SpecError):
+            _run_chain(sv, w, tuning=sv.Tuning(cluster=cluster))
+        return
+    ref = oracle_verify(w)
+    tun = sv.Tuning(cluster=cluster)
+    compare(_run_chain(sv, w, want_alpha=True, tuning=tun), ref, w)
+    assert tun.plan["cluster"] == cluster
+    assert tun.plan["smem_bytes"] == 8 * tun.plan["items"] * 2 * 1024
+    N = 7
+    out = _run_block(sv, w, budget=N, tuning=sv.Tuning(cluster=cluster))
+    a_ref = oracle_alpha(w)
+    np.testing.assert_allclose(to_np(out.alpha), a_ref, atol=1e-5, rtol=0)
+    br = O.alloc_budget(a_ref, N)
+    gdepth = out.depth.cpu().numpy()
+    if not check_budget_choice(gdepth, br.conf, N, br.margin):
+        np.testing.assert_array_equal(gdepth, br.depth)
+    compare(out, oracle_verify(w, depth=gdepth), w)
+    t, d, _, _ = _dev(w)
+    a, _, _ = sv.overlap_alpha(t, d, w.temperature, tuning=sv.Tuning(cluster=cluster))
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(to_np(a), a_ref, atol=1e-5, rtol=0)
+    assert sv.default_workspace().status() == 0
+
+
 @pytest.mark.parametrize("cluster", [1, 2, 4, 8, 16])
 def test_every_cluster_size_bf16(sv, cluster):
     """The same bf16 batch at every cluster size gives the oracle's decisions."""
     w = W.stochastic_mtp(B=6, V=128000)
     ref = oracle_verify(w)
     tun = sv.Tuning(cluster=cluster)
+    if not _slab_fits(128000, 2, cluster):
+        with pytest.raises(sv.SpecError):
+            _run_chain(sv, w, want_alpha=True, tuning=tun)
+        return
     compare(_run_chain(sv, w, want_alpha=True, tuning=tun), ref, w)
     assert tun.plan["cluster"] == cluster
