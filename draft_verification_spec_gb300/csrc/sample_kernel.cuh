@@ -145,6 +145,13 @@ __device__ __forceinline__ void cp_async_wait_upto(int n) {
   }
 }
 
+// Largest value across the warp in one instruction (-inf if every lane holds -inf).
+__device__ __forceinline__ float warp_maxf(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
 __device__ __forceinline__ void lds16(uint32_t* w, uint32_t addr) {
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
@@ -182,6 +189,8 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
   extern __shared__ __align__(128) uint8_t slab[];
   __shared__ __align__(16) float4 mbox1[2][ENT];               // (m_t, s_t, m_d, s_d) per (CTA, warp)
   __shared__ __align__(8) uint64_t x1_bar[2];
+  __shared__ float norm_sh[2];                                 // offt, offd of the current unit
+  __shared__ int mode_sh;
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -363,7 +372,8 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
       U.gd = pair ? static_cast<const uint8_t*>(P.draft) +
                         ((static_cast<size_t>(b) * K + k) * static_cast<size_t>(V) + lo) * ESZ
                   : U.gt;
-      const bool tested = !stats_only && k < K;
+      // the accept test's operands (warp 0 runs it)
+      const bool tested = !stats_only && k < K && warp == 0;
       U.x = (tested && lane == 0) ? __ldg(&P.tokens[static_cast<size_t>(b) * K + k]) : -1;
       U.uk = tested ? __ldg(&P.uniforms[static_cast<size_t>(b) * (K + 1) + k]) : 0.f;
       U.ztx = U.zdx = 0.f;
@@ -371,9 +381,9 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
     }
     return false;
   };
-  // lane 0: the logits at the drafted token
+  // thread 0: the logits at the drafted token
   auto fetch_at_token = [&](SampUnit& U) {
-    if (lane == 0 && U.x >= 0 && U.x < V) {
+    if (tid == 0 && U.x >= 0 && U.x < V) {
       const size_t ot = (static_cast<size_t>(U.b) * (K + 1) + U.k) * V + U.x;
       const size_t od = (static_cast<size_t>(U.b) * K + U.k) * V + U.x;
       if constexpr (BF16) {
@@ -479,6 +489,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
 
   SampUnit A = {};
   bool hasA = take_unit(A);
+  fetch_at_token(A);
   if constexpr (ALIGNED) {
     // the first unit's slice, one commit group per item; pass 2 commits one group per item too,
     // so when pass 1 consumes item it, the groups after it are items it+1 .. nitems-1
@@ -492,7 +503,6 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
   while (hasA) {
     const int apar = A.idx & 1;
     if (tid == 0) mbar_arrive_tx(smem_addr(&x1_bar[apar]), static_cast<uint32_t>(nent) * 16u);
-    fetch_at_token(A);
 
     // ---- pass 1, then the warp partials (warp maximum, every lane's sum rescaled to it) to every
     // CTA of the cluster
@@ -500,7 +510,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
     if (A.pair) pass1(std::true_type(), A, mt, st, md, sd);
     else pass1(std::false_type(), A, mt, st, md, sd);
     {
-      const float wt = warp_max(mt), wd = warp_max(md);
+      const float wt = warp_maxf(mt), wd = warp_maxf(md);
       const float rt = wt == ninf() ? 0.f : wt, rd = wd == ninf() ? 0.f : wd;
       st = warp_sum(st * ex2((mt - rt) * c));
       sd = warp_sum(sd * ex2((md - rd) * c));
@@ -510,65 +520,74 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
       }
     }
 
-    // ---- the row normalisers and the accept test (the barrier carries thread 0's acquire of the
-    // peers' partials to the whole CTA)
-    if (tid == 0) wait_phase(smem_addr(&x1_bar[apar]), (A.idx >> 1) & 1);
-    __syncthreads();
-    float Mt = ninf(), Md = ninf();
-#pragma unroll
-    for (int q = 0; q < EPL; ++q) {
-      const int e = lane * EPL + q;
-      if (e < nent) {
-        const float4 v = mbox1[apar][e];
-        Mt = fmaxf(Mt, v.x);
-        Md = fmaxf(Md, v.z);
-      }
-    }
-    Mt = warp_max(Mt);
-    Md = warp_max(Md);
-    float St = 0.f, Sd = 0.f;
-    {
-      const float rt = (Mt == ninf()) ? 0.f : Mt, rd = (Md == ninf()) ? 0.f : Md;
+    // ---- the next unit (while the exchange completes), then the row normalisers and the accept
+    // test, by warp 0 alone while the other warps wait at the barrier; the barrier carries thread
+    // 0's acquire of the peers' partials and warp 0's results to the whole CTA
+    SampUnit N = {};
+    const bool hasN = take_unit(N);
+    fetch_at_token(N);
+    if (warp == 0) {
+      if (lane == 0) wait_phase(smem_addr(&x1_bar[apar]), (A.idx >> 1) & 1);
+      __syncwarp();
+      float Mt = ninf(), Md = ninf();
 #pragma unroll
       for (int q = 0; q < EPL; ++q) {
         const int e = lane * EPL + q;
         if (e < nent) {
           const float4 v = mbox1[apar][e];
-          St += v.y * ex2((v.x - rt) * c);
-          Sd += v.w * ex2((v.z - rd) * c);
+          Mt = fmaxf(Mt, v.x);
+          Md = fmaxf(Md, v.z);
+        }
+      }
+      Mt = warp_maxf(Mt);
+      Md = warp_maxf(Md);
+      float St = 0.f, Sd = 0.f;
+      {
+        const float rt = (Mt == ninf()) ? 0.f : Mt, rd = (Md == ninf()) ? 0.f : Md;
+#pragma unroll
+        for (int q = 0; q < EPL; ++q) {
+          const int e = lane * EPL + q;
+          if (e < nent) {
+            const float4 v = mbox1[apar][e];
+            St += v.y * ex2((v.x - rt) * c);
+            Sd += v.w * ex2((v.z - rd) * c);
+          }
+        }
+      }
+      St = warp_sum(St);
+      Sd = warp_sum(Sd);
+      if (lane == 0) {
+        // p_v = 2^(z c - offt), q_v = 2^(z c - offd): the normalisers folded into the exponent
+        const float offt = (Mt == ninf() ? 0.f : Mt * c) + lg2f(St);
+        const float offd = (Md == ninf() ? 0.f : Md * c) + lg2f(Sd);
+        float px = 0.f, qx = 0.f;
+        const bool xin = A.x >= 0 && A.x < V;
+        if (xin) {
+          px = ex2(fmaf(A.ztx, c, -offt));
+          qx = ex2(fmaf(A.zdx, c, -offd));
+        }
+        const bool rejects = !stats_only && A.k < K && !(xin && A.uk * qx < px);
+        // a pair that passes the test and draws nothing needs only alpha = sum min(p, q), and
+        // min(2^a, 2^b) = 2^min(a, b): one exp2 per logit pair and no mass table
+        const int mode = A.pair ? ((!rejects && !A.pdraw) ? kModeAlpha : kModeFull) : kModeSingle;
+        norm_sh[0] = offt;
+        norm_sh[1] = offd;
+        mode_sh = mode;
+        if (rank == 0) {
+          UnitRec* r = P.recs + A.rec;
+          r->px = px;
+          r->qx = qx;
+          r->offt = offt;
+          r->offd = offd;
+          r->mode = mode;
         }
       }
     }
-    St = warp_sum(St);
-    Sd = warp_sum(Sd);
-    // p_v = 2^(z c - offt), q_v = 2^(z c - offd): the normalisers folded into the exponent
-    const float offt = (Mt == ninf() ? 0.f : Mt * c) + lg2f(St);
-    const float offd = (Md == ninf() ? 0.f : Md * c) + lg2f(Sd);
-    float px = 0.f, qx = 0.f;
-    const bool xin = lane == 0 && A.x >= 0 && A.x < V;
-    if (xin) {
-      px = ex2(fmaf(A.ztx, c, -offt));
-      qx = ex2(fmaf(A.zdx, c, -offd));
-    }
-    px = __shfl_sync(0xffffffffu, px, 0);
-    qx = __shfl_sync(0xffffffffu, qx, 0);
-    const bool xin_all = __shfl_sync(0xffffffffu, xin ? 1 : 0, 0) != 0;
-    const bool rejects = !stats_only && A.k < K && !(xin_all && A.uk * qx < px);
-    // a pair that passes the test and draws nothing needs only alpha = sum min(p, q), and
-    // min(2^a, 2^b) = 2^min(a, b): one exp2 per logit pair and no mass table
-    const int mode = A.pair ? ((!rejects && !A.pdraw) ? kModeAlpha : kModeFull) : kModeSingle;
-    if (rank == 0 && tid == 0) {
-      UnitRec* r = P.recs + A.rec;
-      r->px = px;
-      r->qx = qx;
-      r->offt = offt;
-      r->offd = offd;
-      r->mode = mode;
-    }
+    __syncthreads();
+    const float offt = norm_sh[0], offd = norm_sh[1];
+    const int mode = mode_sh;
 
     // ---- pass 2, handing the slab over to the next unit item by item
-    SampUnit N = {};
-    const bool hasN = take_unit(N);
     const uint8_t* nT = hasN ? N.gt + wl : nullptr;
     const uint8_t* nD = (hasN && N.pair) ? N.gd + wl : nullptr;
     float* const mrow = P.mass + static_cast<size_t>(A.rec) * kMassRowFloats;

@@ -13,7 +13,7 @@ constexpr int kMaxK = 31;         // drafted positions per request (lanes 0..K o
 // Sampling kernel geometry: 8 warps per CTA; per item every lane loads kSampPieces 16-byte pieces
 // of each row straight into registers.
 #ifndef SPEC_SAMP_PIECES
-#define SPEC_SAMP_PIECES 2
+#define SPEC_SAMP_PIECES 4
 #endif
 #ifndef SPEC_SAMP_MINB
 #define SPEC_SAMP_MINB 3
@@ -24,9 +24,9 @@ constexpr int kSampWarpBytes = kSampPieces * 512;                    // one row,
 constexpr int kSampItemBytes = kSampWarps * kSampWarpBytes;           // one row, one item
 constexpr int kSampMinBlocks = SPEC_SAMP_MINB;                        // resident CTAs per SM the registers allow
 // A CTA's slice of a unit (target and draft row) stays in a shared-memory slab of at most
-// kSampMaxItems items per row between the two passes.
-constexpr int kSampMaxItems = 12;
+// kSampMaxItems items per row (192 KB) between the two passes.
 constexpr int samp_slab_bytes(int items) { return kSampWarps * items * 2 * kSampWarpBytes; }
+constexpr int kSampMaxItems = (192 * 1024) / samp_slab_bytes(1);
 constexpr int kSampMaxSlabBytes = samp_slab_bytes(kSampMaxItems);
 
 // Status bits in the workspace's device status word.

@@ -415,11 +415,10 @@ def test_fp32_multi_cta_chain_block_budget(sv, V, cluster):
 
 
 def _slab_fits(V, esz, cluster):
-    """Whether a CTA slice fits the sampling kernel's shared-memory slab (12 items of 8 KB per row,
-    at most 80 (CTA, item) segments per row)."""
+    """Whether a CTA slice fits the sampling kernel's shared-memory slab (96 KB per row; the shapes
+    tested here stay far below the limit of 80 (CTA, item) segments per row)."""
     slice_ = math.ceil(math.ceil(V / cluster) / 8) * 8
-    items = math.ceil(slice_ * esz / 8192)
-    return items <= 12 and cluster * items <= 80
+    return slice_ * esz <= 96 * 1024
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
@@ -439,7 +438,9 @@ def test_slab_sizes(sv, dtype, V, cluster):
     tun = sv.Tuning(cluster=cluster)
     compare(_run_chain(sv, w, want_alpha=True, tuning=tun), ref, w)
     assert tun.plan["cluster"] == cluster
-    assert tun.plan["smem_bytes"] == 8 * tun.plan["items"] * 2 * 1024
+    slice_bytes = tun.plan["slice"] * esz
+    assert 2 * slice_bytes <= tun.plan["smem_bytes"] <= 192 * 1024                # both rows of the slice fit
+    assert tun.plan["smem_bytes"] % (2 * tun.plan["items"]) == 0
     N = 7
     out = _run_block(sv, w, budget=N, tuning=sv.Tuning(cluster=cluster))
     a_ref = oracle_alpha(w)
