@@ -25,9 +25,11 @@ __device__ __forceinline__ float alpha_of(const BudgetParams& P, int b, int k) {
 }
 
 // One CTA builds the whole confidence table; its warps take requests b = warp, warp + nwarps, ...
-// (grid > 1 only when every CTA can rebuild the table from inputs nobody clears).
+// (grid > 1 only when every CTA can rebuild the table from inputs nobody clears).  The tables are
+// stored position-major ([K][B]), so lanes that read different requests at one position -- or at
+// different positions -- hit different banks.
 __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid_constant__ BudgetParams P) {
-  extern __shared__ float conf[];   // [B, K] prefix confidences, then (sampling path) [B, K] alpha
+  extern __shared__ float conf[];   // [K, B] prefix confidences, then (sampling path) [K, B] alpha
   float* const alpha_s = conf + P.B * P.K;
   asm volatile("griddepcontrol.wait;" ::: "memory");   // the row kernel's results are complete
   const int B = P.B, K = P.K;
@@ -38,18 +40,21 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid
       float cp = 1.f;
       for (int k = 0; k < K; ++k) {
         cp *= fminf(fmaxf(alpha_of(P, b, k), 0.f), 1.f);   // clamp; NaN -> 0
-        conf[b * K + k] = cp;
+        conf[k * B + b] = cp;
       }
     }
   } else {
     // sampling path: every row's alpha in parallel (a thread per row), then the prefix products
-    for (int r = threadIdx.x; r < B * K; r += blockDim.x) alpha_s[r] = alpha_of_row(P, r / K, r - (r / K) * K);
+    for (int r = threadIdx.x; r < B * K; r += blockDim.x) {
+      const int b = r / K, k = r - b * K;
+      alpha_s[k * B + b] = alpha_of_row(P, b, k);
+    }
     __syncthreads();
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
       float cp = 1.f;
       for (int k = 0; k < K; ++k) {
-        cp *= alpha_s[b * K + k];
-        conf[b * K + k] = cp;
+        cp *= alpha_s[k * B + b];
+        conf[k * B + b] = cp;
       }
     }
   }
@@ -58,13 +63,13 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid
     // rank of key (b, m): within each request b' the keys that precede it form a prefix
     // (conf is non-increasing in m'), found by binary search; lanes split the requests.
     auto rank_of = [&](int m) {
-      const float cv = conf[b * K + m];
+      const float cv = conf[m * B + b];
       int cnt = 0;
       for (int bp = lane; bp < B; bp += 32) {
         int lo = 0, hi = K;
         while (lo < hi) {
           const int mid = (lo + hi) >> 1;
-          if (precedes(conf[bp * K + mid], mid, bp, cv, m, b)) lo = mid + 1; else hi = mid;
+          if (precedes(conf[mid * B + bp], mid, bp, cv, m, b)) lo = mid + 1; else hi = mid;
         }
         cnt += lo;
       }
@@ -79,13 +84,13 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid
     const int d = lo;
     if (P.out_depth && lane == 0) P.out_depth[b] = d;
     if (P.out_conf)
-      for (int k = lane; k < K; k += 32) P.out_conf[static_cast<size_t>(b) * K + k] = conf[b * K + k];
+      for (int k = lane; k < K; k += 32) P.out_conf[static_cast<size_t>(b) * K + k] = conf[k * B + b];
     if (P.do_cut) {
       if (P.greedy)
         cut_request(b, d, P.stats_only != 0, P.keys, P.draft_keys != 0, false, P.U, K, P.V, P.tokens,
                     P.out_tokens, P.out_accepted, P.out_alpha, P.out_cum, P.out_E, P.status, lane);
       else
-        cut_sampling(P, b, d, lane, true, lane < K ? alpha_s[b * K + lane] : 0.f);
+        cut_sampling(P, b, d, lane, true, lane < K ? alpha_s[lane * B + b] : 0.f);
     }
   }
   if (P.greedy && P.keys) {   // every warp of the (single) CTA is done with the keys: clear them

@@ -1,5 +1,5 @@
 // The serial cut of one request on the sampling path (T > 0), run by one whole warp after the
-// sampling row kernel: alpha from the per-warp partials, the accept test, the first rejection,
+// sampling row kernel: alpha from the row records, the accept test, the first rejection,
 // and the one draw the request needs -- from norm(max(0, p - q)) at the first rejection, or from
 // p at the verified depth -- located in the row's mass table and resolved by reloading the one
 // segment of logits that owns it.
@@ -51,23 +51,9 @@ __device__ __forceinline__ int cross_entry(const float (&m)[E], float cum0, floa
   return l * E + __shfl_sync(0xffffffffu, first, l);
 }
 
-// alpha_k of request b from its row's ncta * 8 per-warp partials (contiguous, read as float4),
-// summed by one thread in (CTA, warp) order -- every kernel that needs alpha calls this, so all
-// get the same bits -- and clamped to [0, 1] (NaN reads as 0).
+// alpha_k of request b, as the row kernel summed and clamped it into the row's record.
 __device__ __forceinline__ float alpha_of_row(const BudgetParams& P, int b, int k) {
-  const float4* a = reinterpret_cast<const float4*>(P.mass + static_cast<size_t>(b * P.U + k) * kMassRowFloats);
-  const int nq = P.ncta * 2;                 // float4 per row (8 partials per CTA)
-  float s = 0.f;
-  for (int q0 = 0; q0 < nq; q0 += 8) {       // up to eight loads in flight (one round for 4 CTAs)
-    float4 v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (q0 + i < nq) v[i] = __ldcg(a + q0 + i);
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (q0 + i < nq) s = (((s + v[i].x) + v[i].y) + v[i].z) + v[i].w;
-  }
-  return fminf(fmaxf(s, 0.f), 1.f);
+  return __ldcg(&P.recs[static_cast<size_t>(b) * P.U + k].alpha);
 }
 // Lane k of the warp: alpha_k of request b (0 for k >= K); every row in parallel.
 __device__ __forceinline__ float alpha_row_warp(const BudgetParams& P, int b, int lane) {
@@ -102,7 +88,7 @@ __device__ __forceinline__ void cut_sampling(const BudgetParams& P, int b, int d
 
   // the draw at row n: the residual norm(max(0, p - q)) after a rejection (p when it is empty),
   // else p (the bonus)
-  const float* mrow = P.mass + static_cast<size_t>(b * U + n) * kMassRowFloats + kMassAlphaFloats;
+  const float* mrow = P.mass + static_cast<size_t>(b * U + n) * kMassRowFloats;
   const int ncta = P.ncta, itmax = P.itmax, nseg = ncta * itmax;
   const int esz = P.bf16 ? 2 : 4;
   const int IL = kSampItemBytes / esz, WS = kSampWarpBytes / esz, EPP = 16 / esz, PS = 32 * EPP;

@@ -17,8 +17,10 @@
 //   pass 2, from shared memory: per logit p = 2^(z c - offt), q = 2^(z c - offd).  A pair that
 //     passes the test and needs no draw only needs alpha = sum 2^min(a, b) (one exp2 per logit
 //     pair); otherwise every warp writes its (item, warp) masses of r = max(0, p - q) and of p to
-//     the row's mass table.  Every warp writes its alpha partial.  As soon as a lane is done with
-//     an item, it copies its pieces of the next unit's item into the same bytes.
+//     the row's mass table.  As soon as a lane is done with an item, it copies its pieces of the
+//     next unit's item into the same bytes.  Every warp's alpha partial reaches rank 0 with the
+//     next exchange (the last unit's in an exchange of its own), and rank 0 writes the row's alpha,
+//     summed in (CTA, warp) order, to its record.
 // The draws themselves are made by the chained cut kernel from the mass tables.  While a CTA
 // waits on its cluster's exchange, the other CTAs resident on its SM keep HBM busy.  A target row
 // that no draw needs is skipped entirely.  Rows that do not start on 16-byte boundaries are read
@@ -28,7 +30,8 @@
 // then waits once more with a long limit, so the exchange protocol stays consistent and no peer
 // store lands in shared memory after the CTA has left.  Only if that second wait also runs out
 // does the CTA stop waiting (abort mode; results unspecified).  Every phase a CTA arms it also
-// waits for, so on the normal path no peer store can arrive after the CTA has exited.
+// waits for, and the kernel ends with a cluster barrier, so no CTA exits while a store it sent or
+// a store sent to it may still be in flight.
 #pragma once
 
 #include <type_traits>
@@ -168,7 +171,7 @@ struct SampUnit {
   const uint8_t* gd;       // draft row slice (pairs)
   int b, k, rec, idx;      // request, position, record index, needed-unit ordinal of this CTA
   bool pair, pdraw;
-  int x;                   // drafted token (lane 0)
+  int x = -1;              // drafted token (thread 0 of a tested pair; -1 otherwise)
   float uk;                // its accept uniform
   float ztx, zdx;          // target and draft logits at x (lane 0)
 };
@@ -188,6 +191,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
   // the slab: warp w, item it, row r (0 target, 1 draft) at byte ((w * itmax + it) * 2 + r) * WB
   extern __shared__ __align__(128) uint8_t slab[];
   __shared__ __align__(16) float4 mbox1[2][ENT];               // (m_t, s_t, m_d, s_d) per (CTA, warp)
+  __shared__ float abox[2][ENT];                               // rank 0: the previous unit's alpha partials
   __shared__ __align__(8) uint64_t x1_bar[2];
   __shared__ float norm_sh[2];                                 // offt, offd of the current unit
   __shared__ int mode_sh;
@@ -381,9 +385,9 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
     }
     return false;
   };
-  // thread 0: the logits at the drafted token
+  // thread 0: the logits at the drafted token of a tested pair (no other unit reads the draft)
   auto fetch_at_token = [&](SampUnit& U) {
-    if (tid == 0 && U.x >= 0 && U.x < V) {
+    if (tid == 0 && U.pair && U.x >= 0 && U.x < V) {
       const size_t ot = (static_cast<size_t>(U.b) * (K + 1) + U.k) * V + U.x;
       const size_t od = (static_cast<size_t>(U.b) * K + U.k) * V + U.x;
       if constexpr (BF16) {
@@ -467,7 +471,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
 #pragma unroll
         for (int o = 8; o; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
         if ((lane & 15) == 0) {
-          mrow[kMassAlphaFloats + ((static_cast<int>(rank) * itmax + it) * NWARP + warp) * 2 + (lane >> 4)] = keep;
+          mrow[((static_cast<int>(rank) * itmax + it) * NWARP + warp) * 2 + (lane >> 4)] = keep;
           if (hi) pw += keep; else rw += keep;
         }
       }
@@ -487,9 +491,9 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
     }
   };
 
-  SampUnit A = {};
+  SampUnit A;
   bool hasA = take_unit(A);
-  fetch_at_token(A);
+  if (hasA) fetch_at_token(A);
   if constexpr (ALIGNED) {
     // the first unit's slice, one commit group per item; pass 2 commits one group per item too,
     // so when pass 1 consumes item it, the groups after it are items it+1 .. nitems-1
@@ -500,9 +504,27 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
       }
   }
 
+  // alpha of a pair: every warp's partial of unit i travels to rank 0 with the exchange of unit
+  // i + 1 (or a last exchange of its own), where warp 0 sums the partials in (CTA, warp) order
+  bool has_prev = false;
+  float prev_aw = 0.f;
+  int prev_rec = 0;
+  auto alpha_to_record = [&](int par) {
+    float s = 0.f;
+#pragma unroll
+    for (int q = 0; q < EPL; ++q) {
+      const int e = lane * EPL + q;
+      if (e < nent) s += abox[par][e];
+    }
+    s = warp_sum(s);
+    if (lane == 0) P.recs[prev_rec].alpha = fminf(fmaxf(s, 0.f), 1.f);   // NaN -> 0
+  };
+
   while (hasA) {
     const int apar = A.idx & 1;
-    if (tid == 0) mbar_arrive_tx(smem_addr(&x1_bar[apar]), static_cast<uint32_t>(nent) * 16u);
+    if (tid == 0)
+      mbar_arrive_tx(smem_addr(&x1_bar[apar]),
+                     static_cast<uint32_t>(nent) * (rank == 0 && has_prev ? 20u : 16u));
 
     // ---- pass 1, then the warp partials (warp maximum, every lane's sum rescaled to it) to every
     // CTA of the cluster
@@ -518,14 +540,17 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
         const uint32_t dst = smem_addr(&mbox1[apar][rank * NWARP + warp]);
         st_async_v4(peer_addr(dst, lane), wt, st, wd, sd, peer_addr(smem_addr(&x1_bar[apar]), lane));
       }
+      if (has_prev && lane == 0)
+        st_async_f32(peer_addr(smem_addr(&abox[apar][rank * NWARP + warp]), 0), prev_aw,
+                     peer_addr(smem_addr(&x1_bar[apar]), 0));
     }
 
     // ---- the next unit (while the exchange completes), then the row normalisers and the accept
     // test, by warp 0 alone while the other warps wait at the barrier; the barrier carries thread
     // 0's acquire of the peers' partials and warp 0's results to the whole CTA
-    SampUnit N = {};
+    SampUnit N;
     const bool hasN = take_unit(N);
-    fetch_at_token(N);
+    if (hasN) fetch_at_token(N);
     if (warp == 0) {
       if (lane == 0) wait_phase(smem_addr(&x1_bar[apar]), (A.idx >> 1) & 1);
       __syncwarp();
@@ -586,6 +611,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
     __syncthreads();
     const float offt = norm_sh[0], offd = norm_sh[1];
     const int mode = mode_sh;
+    if (rank == 0 && warp == 0 && has_prev) alpha_to_record(apar);
 
     // ---- pass 2, handing the slab over to the next unit item by item
     const uint8_t* nT = hasN ? N.gt + wl : nullptr;
@@ -595,11 +621,29 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
     if (mode == kModeAlpha) aw = pass2(std::integral_constant<int, kModeAlpha>(), offt, offd, mrow, nT, nD);
     else if (mode == kModeFull) aw = pass2(std::integral_constant<int, kModeFull>(), offt, offd, mrow, nT, nD);
     else aw = pass2(std::integral_constant<int, kModeSingle>(), offt, offd, mrow, nT, nD);
-    if (lane == 0) mrow[static_cast<int>(rank) * NWARP + warp] = aw;
+    prev_aw = aw;
+    prev_rec = A.rec;
+    has_prev = true;
+    if (!hasN) {
+      // the last unit's alpha partials, in an exchange of their own (only rank 0 receives and waits)
+      const int i = A.idx + 1, par = i & 1;
+      if (rank == 0 && tid == 0) mbar_arrive_tx(smem_addr(&x1_bar[par]), static_cast<uint32_t>(nent) * 4u);
+      if (lane == 0)
+        st_async_f32(peer_addr(smem_addr(&abox[par][rank * NWARP + warp]), 0), prev_aw,
+                     peer_addr(smem_addr(&x1_bar[par]), 0));
+      if (rank == 0) {
+        if (tid == 0) wait_phase(smem_addr(&x1_bar[par]), (i >> 1) & 1);
+        __syncthreads();
+        if (warp == 0) alpha_to_record(par);
+      }
+    }
     A = N;
     hasA = hasN;
   }
   cp_async_wait<0>();                        // only empty groups remain; retire them before leaving
+  // no CTA leaves while a store it sent into a peer (the last alpha partials) may be in flight;
+  // every wait before this point is bounded, so every CTA of the cluster gets here
+  cluster_sync();
 }
 
 }  // namespace sv

@@ -39,7 +39,8 @@ struct UnitRec {
   float px, qx;      // p_k(x_k), q_k(x_k)
   float offt, offd;  // p_v = 2^(z_T[v] c - offt), q_v = 2^(z_D[v] c - offd)
   int32_t mode;      // pass-2 work done: kModeAlpha, kModeFull or kModeSingle
-  int32_t pad0, pad1, pad2;
+  float alpha;       // sum_v min(p_v, q_v) of a pair, clamped to [0, 1] (written after the next exchange)
+  int32_t pad1, pad2;
 };
 enum : int32_t { kModeAlpha = 0, kModeFull = 1, kModeSingle = 2 };
 
@@ -49,9 +50,8 @@ enum : int32_t { kModeAlpha = 0, kModeFull = 1, kModeSingle = 2 };
 //   m[((c * itmax + it) * 8 + w) * 2]  (R, P): residual mass sum max(0, p - q) and mass sum p of
 //                                      item `it` of warp w of CTA c (full / single rows)
 // in vocabulary order (c, it, w).  The cut kernels sum alpha and draw from these.
-constexpr int kMassAlphaFloats = 16 * 8;                 // clusters of up to 16 CTAs x 8 warps
 constexpr int kMassMaxSegments = 80;                     // CTA x item segments of a row (V * e / 8 KB + 16)
-constexpr int kMassRowFloats = kMassAlphaFloats + kMassMaxSegments * 8 * 2;
+constexpr int kMassRowFloats = kMassMaxSegments * 8 * 2;
 
 // Greedy path: per (request, position) two 64-bit argmax keys (target row, draft row), folded
 // with atomicMax by the argmax kernel and cleared by the kernel that consumes them.
