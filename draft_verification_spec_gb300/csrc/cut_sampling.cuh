@@ -70,6 +70,7 @@ __device__ __forceinline__ void cut_sampling(const BudgetParams& P, int b, int d
   write_stats(b, K, a, P.out_alpha, P.out_cum, P.out_E, lane);
   if (P.stats_only) return;
 
+  const float uK = P.uniforms[static_cast<size_t>(b) * (K + 1) + K];   // the draw's uniform, loaded early
   // the serial accept test u_k q_k(x_k) < p_k(x_k) at positions k < d
   bool ok = true;
   int x = -1;
@@ -134,7 +135,6 @@ __device__ __forceinline__ void cut_sampling(const BudgetParams& P, int b, int d
     Ptot += p;
   }
   const bool resid = n < d && Rtot > 0.f;
-  const float uK = P.uniforms[static_cast<size_t>(b) * (K + 1) + K];
   const float total = resid ? Rtot : Ptot;
   const float t = uK * total;
   // the owner entry in (CTA, item, warp) order
