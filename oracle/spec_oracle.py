@@ -268,6 +268,81 @@ def alloc_budget(alpha, N: int) -> BudgetResult:
     return BudgetResult(depth, c, margin)
 
 
+# --------------------------------------------------------------------------
+# draft-side confidence: the budget chosen before the target forward
+# --------------------------------------------------------------------------
+
+def draft_confidence(draft, tokens, T: float) -> np.ndarray:
+    """q_k(x_k): the probability the draft model gave the token it drafted, [B, K].
+
+    The runtime section of the AngelSpec page selects what to verify from the draft model's
+    output distribution, before the target runs; the per-position confidence read here is
+    q_k(x_k) = softmax(z_D[b, k] / T)[x_k].  At T = 0 the draft distribution is the one-hot
+    at its argmax (lowest index on ties), so q_k(x_k) = [x_k == argmax z_D[b, k]].  A token
+    outside [0, V) has confidence 0.
+    """
+    zd = np.asarray(draft, dtype=np.float64)
+    x = np.asarray(tokens, dtype=np.int64)
+    V = zd.shape[-1]
+    ok = (x >= 0) & (x < V)
+    xi = np.where(ok, x, 0)
+    if T == 0.0:
+        qx = (greedy_argmax(zd) == xi).astype(np.float64)
+    else:
+        qx = np.take_along_axis(softmax(zd, T), xi[..., None], axis=-1)[..., 0]
+    return np.where(ok, qx, 0.0)
+
+
+def draft_budget(draft, tokens, T: float, N: int) -> BudgetResult:
+    """The budget of alloc_budget spent on draft-side prefix confidences prod_{k<=m} q_k(x_k)."""
+    return alloc_budget(draft_confidence(draft, tokens, T), N)
+
+
+# --------------------------------------------------------------------------
+# utility / cost choice of the budget N
+# --------------------------------------------------------------------------
+
+@dataclass
+class AdaptiveResult:
+    N: int                # the chosen budget
+    utility: np.ndarray   # [B*K + 1]: U(N) for every N
+    budget: BudgetResult  # the selection at the chosen N
+    margin: float         # (U(N*) - best U(N), N != N*) / U(N*); inf when there is one candidate
+
+
+def adaptive_budget(alpha, cost_n, cost_t) -> AdaptiveResult:
+    """Choose N online: maximise the expected tokens per unit of verification cost.
+
+    The runtime section of the AngelSpec page spends verification where it pays, against a
+    profiled cost of verifying more positions.  With keys ordered as in alloc_budget and S(N)
+    the sum of the first N prefix confidences (the expected accepted drafts of the selection),
+    a batch of B requests that verifies B + N positions (every request verifies its first
+    emitted position) yields B + S(N) tokens, so
+
+        U(N) = (B + S(N)) / cost(B + N),   N = 0 .. B*K,
+
+    where cost is the piecewise-linear interpolation of the table (cost_n ascending, cost_t),
+    held constant beyond its ends (numpy.interp).  N* is the first N with the largest U.
+    """
+    a = np.clip(np.nan_to_num(np.asarray(alpha, dtype=np.float64), nan=0.0), 0.0, 1.0)
+    B, K = a.shape
+    c, _ = cumulative_alpha(a)
+    bb, mm = np.meshgrid(np.arange(B), np.arange(K), indexing="ij")
+    cf, mf, bf = c.ravel(), mm.ravel(), bb.ravel()
+    ranked = np.lexsort((bf, mf, -cf))       # the key order of alloc_budget
+    S = np.concatenate([[0.0], np.cumsum(cf[ranked])])
+    n_tok = B + np.arange(B * K + 1, dtype=np.float64)
+    cost = np.interp(n_tok, np.asarray(cost_n, dtype=np.float64), np.asarray(cost_t, dtype=np.float64))
+    U = (B + S) / cost
+    N = int(np.argmax(U))
+    if U.size > 1:
+        rest = np.delete(U, N)
+        margin = float((U[N] - rest.max()) / U[N])
+    else:
+        margin = np.inf
+    return AdaptiveResult(N, U, alloc_budget(a, N), margin)
+
+
 def verify_budgeted(target, draft, tokens, uniforms, T: float, N: int):
     """alpha for every position, the budget selection, then verification to depth d_b."""
     alpha, _, _ = overlap_stats(target, draft, T)

@@ -452,9 +452,119 @@ def _onehot_pin(mod):
     return r.alpha[0].tolist() == g["alpha"] and a[0].tolist() == g["alpha"]
 
 
+def _draft_logits(probs):
+    with np.errstate(divide="ignore"):
+        return np.log(np.array(probs, dtype=np.float64))     # ln 0 = -inf: probability 0
+
+
+def _draftconf_pin(mod):
+    """The hand-worked draft-side confidences and budgets (tests/golden/draft_confidence.json)."""
+    g = _load("draft_confidence.json")
+    zd, x = _draft_logits(g["probs_T1"]), np.array(g["tokens"])
+    ok = bool(np.allclose(mod.draft_confidence(zd, x, g["T"]), g["qx"], rtol=0, atol=1e-12))
+    ok &= mod.draft_confidence(zd, x, 0.0).tolist() == g["T0_qx"]
+    ok &= bool(np.allclose(mod.draft_confidence(zd, np.array(g["out_of_range_tokens"]), g["T"]),
+                           g["out_of_range_qx"], rtol=0, atol=1e-12))
+    for N, want in g["depth_by_N"].items():
+        r = mod.draft_budget(zd, x, g["T"], int(N))
+        ok &= r.depth.tolist() == want and bool(np.allclose(r.conf, g["conf"], rtol=0, atol=1e-12))
+    for N, want in g["T0_depth_by_N"].items():
+        ok &= mod.draft_budget(zd, x, 0.0, int(N)).depth.tolist() == want
+    return ok
+
+
+def _adaptive_pin(mod):
+    """The hand-worked utility/cost choices of N (tests/golden/adaptive_budget.json)."""
+    g = _load("adaptive_budget.json")
+    a = np.array(g["alpha"])
+    ok = True
+    for t in g["tables"].values():
+        r = mod.adaptive_budget(a, t["cost_n"], t["cost_t"])
+        ok &= r.N == t["N"] and r.budget.depth.tolist() == t["depth"]
+        if "utility" in t:
+            ok &= bool(np.allclose(r.utility, t["utility"], rtol=0, atol=1e-12))
+            ok &= abs(r.margin - t["margin"]) < 1e-12
+    return ok
+
+
+def _adaptive_brute_pin(mod, seed=5):
+    """N* against exhaustive search over every prefix-closed depth vector (tiny B, K)."""
+    import itertools
+    rng = np.random.default_rng(seed)
+    for _ in range(20):
+        B, K = int(rng.integers(1, 4)), int(rng.integers(1, 4))
+        a = rng.uniform(0, 1, (B, K)) ** 0.5
+        cost_n = np.arange(B, B * (K + 1) + 1, dtype=np.float64)
+        cost_t = np.cumsum(rng.uniform(0.1, 1.0, cost_n.size)) + rng.uniform(0, 3)   # increasing
+        c = np.cumprod(a, axis=1)
+        best = np.full(B * K + 1, -1.0)                  # the best expected tokens at each N
+        for d in itertools.product(range(K + 1), repeat=B):
+            n = sum(d)
+            best[n] = max(best[n], sum(c[b, :d[b]].sum() for b in range(B)))
+        U = (B + best) / np.interp(B + np.arange(B * K + 1), cost_n, cost_t)
+        r = mod.adaptive_budget(a, cost_n, cost_t)
+        if r.N != int(np.argmax(U)) or not np.allclose(r.utility, U, rtol=1e-12, atol=0):
+            return False
+    return True
+
+
+def test_draft_confidence_golden():
+    assert _draftconf_pin(O)
+
+
+def test_draft_confidence_identities():
+    rng = np.random.default_rng(3)
+    zd = rng.normal(0, 2, (3, 4, 50))
+    x = rng.integers(0, 50, (3, 4))
+    q = O.draft_confidence(zd, x, 0.7)
+    # a constant added to a row changes nothing; T scales the logits
+    np.testing.assert_allclose(O.draft_confidence(zd + rng.normal(0, 5, (3, 4, 1)), x, 0.7), q, rtol=1e-12)
+    np.testing.assert_allclose(O.draft_confidence(zd / 0.7, x, 1.0), q, rtol=1e-12)
+    # one vocabulary entry: certainty; the greedy limit of a small temperature is the one-hot
+    assert np.all(O.draft_confidence(zd[..., :1], np.zeros((3, 4), dtype=int), 0.9) == 1.0)
+    zs = zd.copy()
+    zs[np.arange(3)[:, None], np.arange(4)[None, :], x] += 10.0   # the drafted token leads by 10
+    np.testing.assert_allclose(O.draft_confidence(zs, x, 1e-3), O.draft_confidence(zs, x, 0.0), atol=1e-12)
+
+
+def test_draft_confidence_inverse_mean():
+    """E_{x ~ q}[1 / q(x)] = V for a full-support q: the confidence is a normalised probability."""
+    rng = np.random.default_rng(11)
+    V, n = 6, 200000
+    z = rng.normal(0, 1, V)
+    q_true = np.exp(z) / np.exp(z).sum()       # only to draw x; the check uses the oracle's q(x)
+    x = rng.choice(V, size=n, p=q_true)
+    qx = O.draft_confidence(np.broadcast_to(z, (1, n, V)), x[None], 1.0)[0]
+    inv = 1.0 / qx
+    assert abs(inv.mean() - V) < 4 * inv.std() / np.sqrt(n)
+
+
+def test_adaptive_budget_golden():
+    assert _adaptive_pin(O)
+
+
+def test_adaptive_budget_closed_forms():
+    rng = np.random.default_rng(8)
+    a = rng.uniform(0, 1, (5, 4))
+    a[1, 2] = 0.0
+    a[3, 0] = 0.0
+    B, K = a.shape
+    n = np.array([B, B * (K + 1)], dtype=np.float64)
+    # constant cost: every key with positive confidence pays, a zero key adds nothing
+    c = np.cumprod(a, axis=1)
+    assert O.adaptive_budget(a, n, [2.0, 2.0]).N == int((c > 0).sum())
+    # cost proportional to the positions verified: N = 0 is never beaten (confidences <= 1)
+    assert O.adaptive_budget(a, n, n).N == 0
+
+
+def test_adaptive_budget_exhaustive():
+    assert _adaptive_brute_pin(O)
+
+
 def test_pins_pass_on_the_real_oracle():
     assert _hist_pin(O) and _hand_pin(O) and _budget_pin(O) and _greedy_pin(O) and _icdf_pin(O)
     assert _margin_pin(O) and _budget_margin_pin(O) and _onehot_pin(O)
+    assert _draftconf_pin(O) and _adaptive_pin(O) and _adaptive_brute_pin(O)
 
 
 @pytest.mark.parametrize("old,new,pin", [
@@ -482,10 +592,26 @@ def test_pins_pass_on_the_real_oracle():
      "alpha = (g[:, :K] == greedy_argmax(zt[:, :K])).astype(np.float64)", "onehot"),
     ("alpha = (greedy_argmax(zt[:, :K]) == greedy_argmax(zd)).astype(np.float64)",
      "alpha = (greedy_argmax(zt[:, :K]) == greedy_argmax(zt[:, :K])).astype(np.float64)", "onehot"),
+    # draft-side confidence: the draft's top probability instead of the drafted token's; T
+    # ignored; the one-hot at the wrong index
+    ("qx = np.take_along_axis(softmax(zd, T), xi[..., None], axis=-1)[..., 0]",
+     "qx = softmax(zd, T).max(axis=-1)", "draftconf"),
+    ("qx = np.take_along_axis(softmax(zd, T), xi[..., None], axis=-1)[..., 0]",
+     "qx = np.take_along_axis(softmax(zd, 1.0), xi[..., None], axis=-1)[..., 0]", "draftconf"),
+    ("qx = (greedy_argmax(zd) == xi).astype(np.float64)",
+     "qx = (greedy_argmax(-zd) == xi).astype(np.float64)", "draftconf"),
+    # utility: the B first positions forgotten in the yield or in the cost; ties to the largest N
+    ("U = (B + S) / cost", "U = S / cost", "adaptive"),
+    ("n_tok = B + np.arange(B * K + 1, dtype=np.float64)", "n_tok = np.arange(B * K + 1, dtype=np.float64)",
+     "adaptive"),
+    ("N = int(np.argmax(U))", "N = int(U.size - 1 - np.argmax(U[::-1]))", "adaptive"),
+    ("S = np.concatenate([[0.0], np.cumsum(cf[ranked])])", "S = np.concatenate([[0.0], np.cumsum(cf)])",
+     "adaptive_brute"),
 ])
 def test_pins_catch_planted_mistakes(old, new, pin):
     mod = _mutant(old, new)
     check = {"hist": _hist_pin, "hand": _hand_pin, "budget": _budget_pin, "greedy": _greedy_pin,
              "icdf": _icdf_pin, "margin": _margin_pin, "budget_margin": _budget_margin_pin,
-             "onehot": _onehot_pin}[pin]
+             "onehot": _onehot_pin, "draftconf": _draftconf_pin, "adaptive": _adaptive_pin,
+             "adaptive_brute": _adaptive_brute_pin}[pin]
     assert not check(mod)
