@@ -284,5 +284,69 @@ def alloc_budget(alpha, budget: int, stream=None, workspace: Optional[Workspace]
     return depth, conf
 
 
-__all__ = ["verify_chain", "verify_block", "overlap_alpha", "alloc_budget", "Workspace", "VerifyOutput",
-           "Tuning", "SpecError", "lib"]
+def _cost_table(cost, dev):
+    """(cost_n, cost_t) as float32 device tensors on `dev`, or (None, None, 0)."""
+    if cost is None:
+        return None, None, 0
+    cn = torch.as_tensor(cost[0], dtype=torch.float32, device=dev).contiguous()
+    ct = torch.as_tensor(cost[1], dtype=torch.float32, device=dev).contiguous()
+    if cn.dim() != 1 or cn.shape != ct.shape or cn.numel() < 1:
+        raise ValueError("cost must be (cost_n, cost_t): two 1-D sequences of one length >= 1")
+    return cn, ct, cn.numel()
+
+
+def alloc_budget_adaptive(alpha, cost, stream=None, workspace: Optional[Workspace] = None):
+    """The budget with N chosen by utility / cost (spec_alloc_budget_adaptive).
+
+    cost = (cost_n, cost_t): positions verified -> cost, cost_n strictly increasing.  Returns the
+    chosen N (int32 [1]), depth [B] int32 and prefix confidences [B, K].
+    """
+    B, K = alpha.shape
+    _need(alpha, "alpha", dtype=torch.float32, shape=(B, K))
+    dev = alpha.device
+    cn, ct, nc = _cost_table(cost, dev)
+    if nc == 0:
+        raise ValueError("alloc_budget_adaptive needs a cost table")
+    n_out = torch.zeros(1, dtype=torch.int32, device=dev)
+    depth = torch.empty(B, dtype=torch.int32, device=dev)
+    conf = torch.empty(B, K, dtype=torch.float32, device=dev)
+    ws = (workspace or default_workspace(stream))
+    buf = ws.get(B, K, 1, SPEC_F32, stream)
+    _check(lib().spec_alloc_budget_adaptive(_ptr(alpha), B, K, _ptr(cn), _ptr(ct), nc, _ptr(n_out), _ptr(depth),
+                                            _ptr(conf), _ptr(buf), buf.numel(), _stream_ptr(stream)),
+           "spec_alloc_budget_adaptive")
+    return n_out, depth, conf
+
+
+def draft_budget(draft, tokens, temperature: float, budget: Optional[int] = None, cost=None, stream=None,
+                 workspace: Optional[Workspace] = None):
+    """The budget from the draft alone, before the target runs (spec_draft_budget).
+
+    draft [B, K, V] bf16/fp32, tokens [B, K] int32.  Either `budget` (N >= 0) or `cost`
+    ((cost_n, cost_t), N chosen by utility / cost).  Returns N (int32 [1]), depth [B] int32 and
+    the prefix confidences prod q_k(x_k) [B, K].
+    """
+    if draft.dim() != 3:
+        raise ValueError("draft logits must be [B, K, V]")
+    B, K, V = draft.shape
+    dev = draft.device
+    _need(draft, "draft", shape=(B, K, V))
+    code = _dtype_code(draft)
+    _need(tokens, "tokens", dtype=torch.int32, shape=(B, K), device=dev)
+    cn, ct, nc = _cost_table(cost, dev)
+    if nc == 0 and (budget is None or budget < 0):
+        raise ValueError("draft_budget needs budget >= 0 or a cost table")
+    n_out = torch.zeros(1, dtype=torch.int32, device=dev)
+    depth = torch.empty(B, dtype=torch.int32, device=dev)
+    conf = torch.empty(B, K, dtype=torch.float32, device=dev)
+    ws = (workspace or default_workspace(stream))
+    buf = ws.get(B, K, V, code, stream)
+    _check(lib().spec_draft_budget(_ptr(draft), code, _ptr(tokens), B, K, V, float(temperature),
+                                   -1 if budget is None else int(budget), _ptr(cn), _ptr(ct), nc, _ptr(n_out),
+                                   _ptr(depth), _ptr(conf), _ptr(buf), buf.numel(), _stream_ptr(stream)),
+           "spec_draft_budget")
+    return n_out, depth, conf
+
+
+__all__ = ["verify_chain", "verify_block", "overlap_alpha", "alloc_budget", "alloc_budget_adaptive",
+           "draft_budget", "Workspace", "VerifyOutput", "Tuning", "SpecError", "lib"]

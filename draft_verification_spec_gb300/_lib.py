@@ -37,6 +37,10 @@ SIGNATURES = {
                                    c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "spec_alloc_budget": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p, c_size_t,
                                   c_void_p]),
+    "spec_alloc_budget_adaptive": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_int, c_void_p,
+                                           c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "spec_draft_budget": (c_int, [c_void_p, c_int, c_void_p, c_int, c_int, c_int, c_float, c_int, c_void_p,
+                                  c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "spec_verify_chain_greedy_static": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int, c_int,
                                                 c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "spec_verify_tuned": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int, c_int, c_int,

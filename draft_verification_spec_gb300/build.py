@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspecverify.so")
-SOURCES = ["row_bf16.cu", "row_f32.cu", "budget_cut.cu", "api.cu", "static_scratch.cu"]
+SOURCES = ["row_bf16.cu", "row_f32.cu", "budget_cut.cu", "draft_conf.cu", "api.cu", "static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -650,4 +650,93 @@ spec_status_t spec_alloc_budget(const float* alpha, int B, int K, int budget_N, 
                                                                                       : SPEC_ERR_CUDA;
 }
 
+spec_status_t spec_alloc_budget_adaptive(const float* alpha, int B, int K, const float* cost_n,
+                                         const float* cost_t, int n_cost, int32_t* out_N, int32_t* out_depth,
+                                         float* out_conf, void* workspace, size_t ws_bytes, void* stream) {
+  if (B < 0 || K < 0 || n_cost < 1) return SPEC_ERR_INVALID_ARG;
+  if (n_cost > sv::kBudgetMaxCost) return SPEC_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * K > kBudgetMaxKeys) return SPEC_ERR_UNSUPPORTED;
+  if (B == 0) return SPEC_OK;
+  if (!out_depth || !cost_n || !cost_t || (K > 0 && !alpha)) return SPEC_ERR_INVALID_ARG;
+  spec_status_t st = check_ws(workspace, ws_bytes, B, K);
+  if (st != SPEC_OK) return st;
+  sv::BudgetParams bp;
+  std::memset(&bp, 0, sizeof(bp));
+  bp.alpha_in = alpha;
+  bp.B = B;
+  bp.K = K;
+  bp.do_cut = 0;
+  bp.cost_n = cost_n;
+  bp.cost_t = cost_t;
+  bp.n_cost = n_cost;
+  bp.out_N = out_N;
+  bp.out_depth = out_depth;
+  bp.out_conf = out_conf;
+  bp.status = static_cast<int32_t*>(workspace);
+  return sv::launch_budget_cut(bp, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status_t spec_draft_budget(const void* draft_logits, int dtype, const int32_t* tokens, int B, int K, int V,
+                                float temperature, int budget_N, const float* cost_n, const float* cost_t,
+                                int n_cost, int32_t* out_N, int32_t* out_depth, float* out_conf,
+                                void* workspace, size_t ws_bytes, void* stream) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+  if (B < 0 || K < 0 || V < 1 || bad_T(temperature) || n_cost < 0) return SPEC_ERR_INVALID_ARG;
+  if (n_cost == 0 && budget_N < 0) return SPEC_ERR_INVALID_ARG;
+  if (n_cost > sv::kBudgetMaxCost || V > kMaxV) return SPEC_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * K > kBudgetMaxKeys) return SPEC_ERR_UNSUPPORTED;
+  if (B == 0) return SPEC_OK;
+  if (!out_depth || (n_cost > 0 && (!cost_n || !cost_t)) || (K > 0 && (!draft_logits || !tokens)))
+    return SPEC_ERR_INVALID_ARG;
+  spec_status_t st = check_ws(workspace, ws_bytes, B, K);
+  if (st != SPEC_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool bf16 = dtype == SPEC_BF16;
+  const int esz = bf16 ? 2 : 4;
+  const bool greedy = temperature == 0.f;
+  const float c = greedy ? 0.f : static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  // the partials of every draft row live in the workspace's mass tables (at most 16 x 16 B a row)
+  const WsLayout L = ws_layout_for(ws_bytes);
+  float4* part = reinterpret_cast<float4*>(static_cast<uint8_t*>(workspace) + L.mass);
+  int nparts = static_cast<int>((static_cast<size_t>(V) * esz + 65535) / 65536);
+  nparts = nparts < 1 ? 1 : (nparts > 16 ? 16 : nparts);
+  const int part_len = static_cast<int>(align_up((V + nparts - 1) / nparts, sv::kChunk));
+  nparts = (V + part_len - 1) / part_len;
+  if (K > 0) {
+    sv::DraftStatsParams dp;
+    dp.draft = draft_logits;
+    dp.rows = B * K;
+    dp.V = V;
+    dp.nparts = nparts;
+    dp.part_len = part_len;
+    dp.c = c;
+    dp.out = part;
+    const bool aligned = (static_cast<size_t>(V) * esz) % 16 == 0 && aligned16(draft_logits);
+    if (sv::launch_draft_stats(bf16, greedy, aligned, dp, s) != cudaSuccess) return SPEC_ERR_CUDA;
+  }
+  sv::BudgetParams bp;
+  std::memset(&bp, 0, sizeof(bp));
+  bp.draft_part = part;
+  bp.nparts = nparts;
+  bp.draft_greedy = greedy ? 1 : 0;
+  bp.draft = draft_logits;
+  bp.bf16 = bf16 ? 1 : 0;
+  bp.c = c;
+  bp.tokens = tokens;
+  bp.U = K + 1;
+  bp.B = B;
+  bp.K = K;
+  bp.V = V;
+  bp.N = budget_N;
+  bp.do_cut = 0;
+  bp.cost_n = cost_n;
+  bp.cost_t = cost_t;
+  bp.n_cost = n_cost;
+  bp.out_N = out_N;
+  bp.out_depth = out_depth;
+  bp.out_conf = out_conf;
+  bp.status = static_cast<int32_t*>(workspace);
+  return sv::launch_budget_cut(bp, s) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
 }  // extern "C"

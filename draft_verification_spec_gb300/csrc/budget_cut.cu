@@ -24,13 +24,137 @@ __device__ __forceinline__ float alpha_of(const BudgetParams& P, int b, int k) {
   return key_index(__ldcg(kb)) == key_index(__ldcg(kb + 1)) ? 1.f : 0.f;
 }
 
+// q_k(x_k) of request b from the draft statistics kernel's partials of row (b, k), merged in part
+// order: 2^((z_x - M) c) / S, or [x_k == first argmax] at T = 0; 0 for a token outside [0, V).
+__device__ __forceinline__ float draft_q(const BudgetParams& P, int b, int k) {
+  const size_t r = static_cast<size_t>(b) * P.K + k;
+  const int x = P.tokens[r];
+  if (x < 0 || x >= P.V) return 0.f;
+  const float4* pr = P.draft_part + r * P.nparts;
+  float M = ninf();
+  for (int j = 0; j < P.nparts; ++j) M = fmaxf(M, __ldcg(&pr[j].x));
+  if (P.draft_greedy) {
+    unsigned I = 0xffffffffu;
+    for (int j = 0; j < P.nparts; ++j)
+      if (__ldcg(&pr[j].x) == M) I = min(I, __float_as_uint(__ldcg(&pr[j].z)));
+    return static_cast<unsigned>(x) == I ? 1.f : 0.f;
+  }
+  const float ref = M == ninf() ? 0.f : M;
+  float S = 0.f;
+  for (int j = 0; j < P.nparts; ++j) S += __ldcg(&pr[j].y) * ex2((__ldcg(&pr[j].x) - ref) * P.c);
+  const void* row = static_cast<const uint8_t*>(P.draft) + r * P.V * (P.bf16 ? 2 : 4);
+  const float q = ex2((logit_at(row, x, P.bf16 != 0) - ref) * P.c) / S;
+  return fminf(fmaxf(q, 0.f), 1.f);   // NaN (a row with no finite logit) -> 0
+}
+
+// The cost of verifying n positions: the table interpolated piecewise-linearly, held constant
+// beyond its ends.
+__device__ __forceinline__ float cost_at(float n, const float* cn, const float* ct, int nc) {
+  if (n <= cn[0]) return ct[0];
+  if (n >= cn[nc - 1]) return ct[nc - 1];
+  int i = 0;
+  while (i + 2 < nc && cn[i + 1] <= n) ++i;
+  return ct[i] + (ct[i + 1] - ct[i]) * (n - cn[i]) / (cn[i + 1] - cn[i]);
+}
+
+// The budget N with the largest expected tokens per unit of verification cost: the first N
+// maximising (B + S(N)) / cost(B + N), S(N) the sum of the N largest prefix confidences.  Every
+// thread of the CTA calls it and gets the same N (the confidences are sorted in shared memory:
+// bitonic sort, descending; then one scan).
+__device__ int choose_budget(const BudgetParams& P, const float* conf, float* sb, float* cn, float* ct,
+                             float* red_u, int* red_n, int* n_out) {
+  const int BK = P.B * P.K, tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
+  const int nw = nt >> 5;
+  int n2 = 1;
+  while (n2 < BK) n2 <<= 1;
+  for (int i = tid; i < n2; i += nt) sb[i] = i < BK ? conf[i] : -1.f;
+  for (int i = tid; i < P.n_cost; i += nt) {
+    cn[i] = P.cost_n[i];
+    ct[i] = P.cost_t[i];
+  }
+  __syncthreads();
+  for (int k = 2; k <= n2; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < n2; i += nt) {
+        const int l = i ^ j;
+        if (l > i) {
+          const float a = sb[i], bv = sb[l];
+          if (((i & k) == 0) ? a < bv : a > bv) {
+            sb[i] = bv;
+            sb[l] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  // S(N): each thread sums a contiguous run of the sorted values; a scan of the runs' totals
+  const int per = (BK + nt - 1) / nt;
+  const int i0 = min(BK, tid * per), i1 = min(BK, i0 + per);
+  float run = 0.f;
+  for (int i = i0; i < i1; ++i) run += sb[i];
+  const float incl = warp_incl_scan(run, lane);
+  if (lane == 31) red_u[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const float t = lane < nw ? red_u[lane] : 0.f;
+    const float ti = warp_incl_scan(t, lane);
+    if (lane < nw) red_u[lane] = ti - t;
+  }
+  __syncthreads();
+  float S = red_u[warp] + incl - run;
+  float bu = ninf();
+  int bn = 0x7fffffff;
+  auto consider = [&](int N, float SN) {
+    const float u = (static_cast<float>(P.B) + SN) / cost_at(static_cast<float>(P.B + N), cn, ct, P.n_cost);
+    if (u > bu || (u == bu && N < bn)) {
+      bu = u;
+      bn = N;
+    }
+  };
+  if (tid == 0) consider(0, 0.f);
+  for (int i = i0; i < i1; ++i) {
+    S += sb[i];
+    consider(i + 1, S);
+  }
+  // the largest utility, then the smallest N
+  for (int o = 16; o; o >>= 1) {
+    const float ou = __shfl_xor_sync(0xffffffffu, bu, o);
+    const int on = __shfl_xor_sync(0xffffffffu, bn, o);
+    if (ou > bu || (ou == bu && on < bn)) {
+      bu = ou;
+      bn = on;
+    }
+  }
+  __syncthreads();   // every thread is done with the scan offsets in red_u
+  if (lane == 0) {
+    red_u[warp] = bu;
+    red_n[warp] = bn;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float u = red_u[0];
+    int n = red_n[0];
+    for (int w = 1; w < nw; ++w)
+      if (red_u[w] > u || (red_u[w] == u && red_n[w] < n)) {
+        u = red_u[w];
+        n = red_n[w];
+      }
+    *n_out = n;
+  }
+  __syncthreads();
+  return *n_out;
+}
+
 // One CTA builds the whole confidence table; its warps take requests b = warp, warp + nwarps, ...
 // (grid > 1 only when every CTA can rebuild the table from inputs nobody clears).  The tables are
 // stored position-major ([K][B]), so lanes that read different requests at one position -- or at
 // different positions -- hit different banks.
 __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid_constant__ BudgetParams P) {
-  extern __shared__ float conf[];   // [K, B] prefix confidences, then (sampling path) [K, B] alpha
+  // [K, B] prefix confidences, [K, B] per-position confidences; then, for the utility / cost
+  // choice of N, the sort buffer (next power of two >= B K), the cost table and reduction slots
+  extern __shared__ float conf[];
   float* const alpha_s = conf + P.B * P.K;
+  __shared__ int n_choice;
   asm volatile("griddepcontrol.wait;" ::: "memory");   // the row kernel's results are complete
   const int B = P.B, K = P.K;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -44,10 +168,11 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid
       }
     }
   } else {
-    // sampling path: every row's alpha in parallel (a thread per row), then the prefix products
+    // sampling path (alpha from the row records) or draft-side confidences: every row in
+    // parallel (a thread per row), then the prefix products
     for (int r = threadIdx.x; r < B * K; r += blockDim.x) {
       const int b = r / K, k = r - b * K;
-      alpha_s[k * B + b] = alpha_of_row(P, b, k);
+      alpha_s[k * B + b] = P.draft_part ? draft_q(P, b, k) : alpha_of_row(P, b, k);
     }
     __syncthreads();
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
@@ -59,6 +184,18 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid
     }
   }
   __syncthreads();
+  int Nsel = P.N;
+  if (P.n_cost > 0) {
+    int n2 = 1;
+    while (n2 < B * K) n2 <<= 1;
+    float* const sb = conf + 2 * B * K;
+    float* const cn = sb + n2;
+    float* const ct = cn + kBudgetMaxCost;
+    float* const red_u = ct + kBudgetMaxCost;
+    int* const red_n = reinterpret_cast<int*>(red_u + 32);
+    Nsel = choose_budget(P, conf, sb, cn, ct, red_u, red_n, &n_choice);
+    if (blockIdx.x == 0 && threadIdx.x == 0 && P.out_N) *P.out_N = Nsel;
+  }
   for (int b = blockIdx.x * nw + warp; b < B; b += gridDim.x * nw) {
     // rank of key (b, m): within each request b' the keys that precede it form a prefix
     // (conf is non-increasing in m'), found by binary search; lanes split the requests.
@@ -79,7 +216,7 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid
     int lo = 0, hi = K;
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
-      if (rank_of(mid) < P.N) lo = mid + 1; else hi = mid;
+      if (rank_of(mid) < Nsel) lo = mid + 1; else hi = mid;
     }
     const int d = lo;
     if (P.out_depth && lane == 0) P.out_depth[b] = d;
@@ -136,7 +273,12 @@ cudaError_t launch_budget_cut(const BudgetParams& p, cudaStream_t stream, bool p
   // the greedy path clears the keys it reads, so one CTA must own the whole table; otherwise every
   // CTA builds the table and a warp cuts one request
   const int grid = (p.greedy && p.keys) ? 1 : (p.B + per - 1) / per;
-  const size_t smem = static_cast<size_t>(p.B) * p.K * sizeof(float) * ((p.greedy || p.alpha_in) ? 1 : 2);
+  size_t smem = static_cast<size_t>(p.B) * p.K * sizeof(float) * 2;
+  if (p.n_cost > 0) {
+    size_t n2 = 1;
+    while (n2 < static_cast<size_t>(p.B) * p.K) n2 <<= 1;
+    smem += (n2 + 2 * kBudgetMaxCost + 64) * sizeof(float);
+  }
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(budget_cut_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));

@@ -29,6 +29,12 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 // Butterfly sum: every lane ends with the same value (fp add is commutative).
+// Largest value across the warp in one instruction (-inf if every lane holds -inf).
+__device__ __forceinline__ float warp_maxf(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

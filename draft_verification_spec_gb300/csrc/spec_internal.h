@@ -135,9 +135,30 @@ struct BudgetParams {
   float* out_cum;
   float* out_E;
   int32_t* status;
+  // draft-side confidence: per-row partials of the draft statistics kernel (alpha_k is then
+  // q_k(x_k), read from the draft row), or null
+  const float4* draft_part;  // [B*K, nparts]: (max, sum of 2^((z - max) c), first argmax index, 0)
+  int nparts;
+  int draft_greedy;          // T = 0: q_k(x_k) = [x_k == argmax]
+  // the utility / cost choice of N (n_cost > 0; N is then ignored)
+  const float* cost_n;       // [n_cost] strictly increasing
+  const float* cost_t;       // [n_cost]
+  int n_cost;
+  int32_t* out_N;            // the chosen N, or null
 };
 
+// Per-row partials of the draft rows alone: one CTA per (row, part) of part_len logits.
+struct DraftStatsParams {
+  const void* draft;         // [rows, V]
+  int rows, V, nparts, part_len;
+  float c;                   // log2(e) / T (unused at T = 0)
+  float4* out;               // [rows, nparts]
+};
+constexpr int kDraftStatsThreads = 256;
+constexpr int kBudgetMaxCost = 64;     // cost-table points
+
 // Host-side launchers of the small kernels (defined next to them).
+cudaError_t launch_draft_stats(bool bf16, bool greedy, bool aligned, const DraftStatsParams& p, cudaStream_t stream);
 cudaError_t launch_argmax(bool bf16, const ArgmaxParams& p, int grid, cudaStream_t stream);
 cudaError_t argmax_blocks_per_sm(bool bf16, int* out);
 cudaError_t launch_budget_cut(const BudgetParams& p, cudaStream_t stream, bool pdl = true);

@@ -175,6 +175,50 @@ spec_status_t spec_alloc_budget(const float* alpha, int B, int K, int budget_N,
                                 void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * The budget with N chosen online (AngelSpec, section on verification as a
+ * shared pool: verification is spent where it pays against a profiled cost
+ * of verifying more positions).  With the keys and selection of
+ * spec_alloc_budget and S(N) the sum of the N largest prefix confidences,
+ * N = the first N in 0 .. B*K maximising
+ *     (B + S(N)) / cost(B + N),
+ * B + N being the positions the batch verifies (every request verifies its
+ * first emitted position).  cost is the table (cost_n [n_cost] strictly
+ * increasing, cost_t [n_cost]; device, float32) interpolated piecewise-
+ * linearly and held constant beyond its ends.  1 <= n_cost <= 64.
+ * out_N (device int32, nullable) receives N; out_depth and out_conf as in
+ * spec_alloc_budget.  B * K <= 8192.
+ */
+spec_status_t spec_alloc_budget_adaptive(const float* alpha, int B, int K,
+                                         const float* cost_n, const float* cost_t, int n_cost,
+                                         int32_t* out_N, int32_t* out_depth, float* out_conf,
+                                         void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * The budget chosen from the draft alone, before the target runs (AngelSpec,
+ * section on verification as a shared pool: the budget is decided from the
+ * draft model's output distribution).  The confidence of drafted position
+ * (b, k) is q_k(x_k) = softmax(draft_logits[b, k] / T)[tokens[b, k]] (at
+ * T == 0 the one-hot [tokens[b, k] == argmax], lowest index on ties; 0 for a
+ * token outside [0, V)), and the keys are its prefix products
+ * c[b, m] = prod_{k<=m} q_k(x_k), selected as in spec_alloc_budget: with
+ * n_cost == 0 the first min(budget_N, B*K) keys (budget_N >= 0), with
+ * n_cost > 0 the N of spec_alloc_budget_adaptive (budget_N ignored).
+ *   draft_logits  device [B, K, V], dtype SPEC_BF16 or SPEC_F32; one pass
+ *   tokens        device int32 [B, K]
+ *   out_N         device int32 or NULL: the N spent
+ *   out_depth     device int32 [B]: per-request verification depth d_b
+ *   out_conf      device float32 [B, K] or NULL: the prefix confidences
+ * The caller then runs the target on the selected depths and verifies with
+ * spec_verify_chain / spec_verify_block and `depth`.  B * K <= 8192.
+ * Workspace as for spec_verify_block (spec_workspace_bytes(B, K, V, dtype)).
+ */
+spec_status_t spec_draft_budget(const void* draft_logits, int dtype, const int32_t* tokens,
+                                int B, int K, int V, float temperature, int budget_N,
+                                const float* cost_n, const float* cost_t, int n_cost,
+                                int32_t* out_N, int32_t* out_depth, float* out_conf,
+                                void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * Greedy (T == 0) chain verification that allocates nothing and needs no
  * workspace.  The pages have no counterpart: this entry point exists for
  * callers that cannot give the library device memory -- serving engines that

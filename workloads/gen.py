@@ -159,6 +159,17 @@ def random_case(seed: int, B: int, K: int, V: int, T: float, dtype=torch.float32
     return _finish(f"random_{B}x{K}x{V}", zt, zd, dtype, T, _gen(seed + 1000), _gen(seed + 2000))
 
 
+def verify_cost_table(B: int, K: int, points: int = 9):
+    """A synthetic cost profile of verifying n positions in one target forward (arbitrary units),
+    standing in for the profiled table a serving system would measure: flat up to 4 positions per
+    request (the forward is bound by reading weights), then rising with n (bound by compute).
+    Returns (n, cost) as float lists, n from B to B * (K + 1)."""
+    lo, hi = float(B), float(B * (K + 1))
+    n = [lo + (hi - lo) * i / (points - 1) for i in range(points)]
+    knee = 4.0 * B
+    return n, [1.0 + 0.02 * x / B + max(0.0, x - knee) * 0.25 / B for x in n]
+
+
 CONFIGS = {
     "tiny_chain": tiny_chain,
     "greedy_mtp": greedy_mtp,
