@@ -49,6 +49,9 @@ KERNELS = {
     "greedy": {"name": "sv::argmax_kernel<bf16> (argmax + fused cut, one launch)",
                "sources": ["argmax_kernel.cuh", "spec_device.cuh", "spec_internal.h", "budget_cut.cu", "api.cu"],
                "traffic": os.path.join(ROOT, "profiles", "argmax_kernel_traffic.txt")},
+    "draft": {"name": "sv::draft_stats_kernel<bf16> (then sv::budget_cut_kernel, PDL-chained)",
+              "sources": ["draft_conf.cu", "packed_math.cuh", "spec_device.cuh", "spec_internal.h", "api.cu"],
+              "traffic": os.path.join(ROOT, "profiles", "draft_stats_kernel_traffic.txt")},
     "sampling": {"name": "sv::sample_kernel<bf16> (then sv::cut_kernel / sv::budget_cut_kernel, PDL-chained)",
                  "sources": ["sample_kernel.cuh", "spec_async.cuh", "spec_device.cuh", "spec_internal.h", "row_bf16.cu", "api.cu"],
                  "traffic": os.path.join(ROOT, "profiles", "sample_kernel_traffic.txt")},
@@ -175,7 +178,8 @@ def make_workload(name: str, rank: int):
         return W.stochastic_mtp(seed=2 + 100 * rank)
     if name == "dfly_block":
         return W.dfly_block(seed=3 + 100 * rank)
-    if name.startswith("budget_sweep"):
+    if name.startswith("budget_sweep") or name.startswith("draft_budget"):
+        # draft_budget*: the budget sweep's draft rows, the budget chosen before the target runs
         B = int(name.split("_B")[-1]) if "_B" in name else 64
         return W.budget_sweep(B, seed=4 + 100 * rank)
     if name == "tiny_chain":
@@ -185,6 +189,10 @@ def make_workload(name: str, rank: int):
 
 def call_kind(w, name):
     """(entry point, reads draft?) for a workload, matching its configuration."""
+    if name.startswith("draft_budget_adaptive"):
+        return "draft_adaptive", True
+    if name.startswith("draft_budget"):
+        return "draft", True
     if name == "greedy_mtp":
         return "chain", False
     if name in ("stochastic_mtp", "tiny_chain"):
@@ -197,8 +205,11 @@ def verified_tokens(w) -> int:
     return min(w.budget, w.B * w.K) if w.budget is not None else w.B * w.K
 
 
-def algorithmic_bytes(w, reads_draft: bool) -> int:
+def algorithmic_bytes(w, reads_draft: bool, kind: str = "") -> int:
     """Bytes the outputs depend on: logits read once + ids/uniforms read + outputs written."""
+    if kind.startswith("draft"):
+        # the draft rows once, the drafted tokens, depth, prefix confidences and N
+        return w.B * w.K * w.V * w.draft.element_size() + w.B * w.K * 4 + w.B * 4 + w.B * w.K * 4 + 4
     e = w.target.element_size()
     B, K, V = w.B, w.K, w.V
     b = B * (K + 1) * V * e + (B * K * V * e if reads_draft else 0)
@@ -240,13 +251,16 @@ class DeviceRunner:
         import torch
         import draft_verification_spec_gb300 as sv
         self.sv, self.torch, self.w, self.name, self.dev = sv, torch, w, name, device
+        import workloads as W
         self.kind, self.reads_draft = call_kind(w, name)
-        per = w.target.numel() * w.target.element_size() + (
+        self.draft_only = self.kind.startswith("draft")
+        per = (0 if self.draft_only else w.target.numel() * w.target.element_size()) + (
             w.draft.numel() * w.draft.element_size() if self.reads_draft else 0)
+        self.logit_bytes = per
         self.nsets = max(1, math.ceil(min_bytes / per))
         self.sets = []
         for _ in range(self.nsets):
-            t = w.target.to(device)
+            t = None if self.draft_only else w.target.to(device)
             d = w.draft.to(device) if self.reads_draft else None
             self.sets.append((t, d, w.tokens.to(device), w.uniforms.to(device)))
         B, K = w.B, w.K
@@ -257,15 +271,23 @@ class DeviceRunner:
                                    f(B) if block else None, i(B) if w.budget is not None else None)
         self.stream = torch.cuda.Stream(device)
         self.ws = sv.Workspace(device)
-        self.bytes_per_step = algorithmic_bytes(w, self.reads_draft)
+        self.bytes_per_step = algorithmic_bytes(w, self.reads_draft, self.kind)
         self.greedy_fused = w.temperature == 0 and w.budget is None
-        self.kernel_kind = "greedy" if w.temperature == 0 else "sampling"
+        self.kernel_kind = "draft" if self.draft_only else ("greedy" if w.temperature == 0 else "sampling")
+        if self.draft_only:
+            self.dout = (torch.zeros(1, dtype=torch.int32, device=device), i(B), f(B, K))
+            cn, ct = W.verify_cost_table(B, K)
+            self.cost = (torch.tensor(cn, dtype=torch.float32, device=device),
+                         torch.tensor(ct, dtype=torch.float32, device=device)) if self.kind == "draft_adaptive" else None
         self.graphs = {}
 
     def step(self, i, tuning=None):
         t, d, x, u = self.sets[i % self.nsets]
         w, sv = self.w, self.sv
-        if self.kind == "chain":
+        if self.draft_only:
+            sv.draft_budget(d, x, w.temperature, budget=None if self.cost else w.budget, cost=self.cost,
+                            stream=self.stream, workspace=self.ws, out=self.dout)
+        elif self.kind == "chain":
             sv.verify_chain(t, d, x, u, w.temperature, want_alpha=False, stream=self.stream,
                             workspace=self.ws, out=self.out, tuning=tuning)
         else:
@@ -277,7 +299,7 @@ class DeviceRunner:
         events on the launching stream: start, the library's split event between the two launches,
         stop (the chained kernel then runs without programmatic dependent launch)."""
         torch = self.torch
-        if self.greedy_fused:
+        if self.greedy_fused or self.draft_only:
             return None
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
                torch.cuda.Event(enable_timing=True)) for _ in range(n)]
@@ -301,6 +323,8 @@ class DeviceRunner:
         """One call with every statistic requested: realised mean alpha and accepted length."""
         torch, sv, w = self.torch, self.sv, self.w
         t, d, x, u = self.sets[0]
+        if self.draft_only:
+            return None
         with torch.cuda.stream(self.stream):
             if self.kind == "chain":
                 out = sv.verify_chain(t, w.draft.to(self.dev) if d is None and w.K > 0 else d, x, u, w.temperature,
@@ -310,6 +334,14 @@ class DeviceRunner:
                                       stream=self.stream, workspace=self.ws)
         self.stream.synchronize()
         return out
+
+    def tokens_per_step(self):
+        """Positions a step selects for verification: the N of the last call for the adaptive
+        draft-side budget, else verified_tokens."""
+        if self.kind == "draft_adaptive":
+            self.stream.synchronize()
+            return int(self.dout[0].item())
+        return verified_tokens(self.w)
 
     def launches_per_step(self):
         # greedy without a budget: one argmax kernel with the cut fused in; otherwise the row
@@ -418,10 +450,11 @@ def run_gpu(args, rank, local_rank, world):
                 bx = rx.bytes_per_step
                 sx = rx.split(100)
                 tk = sx["row_kernel_us"] / 1e6 if sx else t
-                extra[name] = {"verified_tokens_per_s": verified_tokens(wx) / t,
+                extra[name] = {"verified_tokens_per_s": rx.tokens_per_step() / t,
                                "drafted_tokens_per_s": wx.B * wx.K / t,
-                               "rows_per_s": wx.B * (2 * wx.K + 1) / t,
-                               "us_per_step": t * 1e6, "logit_bytes": wx.logits_bytes(rx.reads_draft),
+                               "rows_per_s": wx.B * (wx.K if rx.draft_only else 2 * wx.K + 1) / t,
+                               "us_per_step": t * 1e6, "tokens_per_step": rx.tokens_per_step(),
+                               "logit_bytes": rx.logit_bytes,
                                "algorithmic_bytes": bx,
                                "achieved_gbs_step": bx / t / 1e9, "frac_of_measured_hbm_step": bx / t / 1e9 / peak_gbs,
                                "achieved_gbs_kernel": bx / tk / 1e9, "frac_of_measured_hbm_kernel": bx / tk / 1e9 / peak_gbs,
@@ -482,6 +515,8 @@ def run_gpu(args, rank, local_rank, world):
 
 def decision_stats(w, out, step_s):
     """Realised statistics of one call's decisions (GPU outputs only)."""
+    if out is None:
+        return None
     acc = out.accepted.double().cpu()
     st = {"mean_accepted": float(acc.mean()), "mean_emitted": float(acc.mean()) + 1.0,
           "acceptance_rate": float(acc.sum()) / max(1, (int(out.depth.sum()) if out.depth is not None
@@ -679,7 +714,8 @@ def parse(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="budget_sweep_B64")
     ap.add_argument("--extra", nargs="*", default=["greedy_mtp", "stochastic_mtp", "dfly_block", "budget_sweep_B4",
-                                                   "budget_sweep_B16", "budget_sweep_B64"])
+                                                   "budget_sweep_B16", "budget_sweep_B64", "draft_budget_B64",
+                                                   "draft_budget_adaptive_B64"])
     ap.add_argument("--extra-steps", type=int, default=3000)
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")

@@ -319,12 +319,13 @@ def alloc_budget_adaptive(alpha, cost, stream=None, workspace: Optional[Workspac
 
 
 def draft_budget(draft, tokens, temperature: float, budget: Optional[int] = None, cost=None, stream=None,
-                 workspace: Optional[Workspace] = None):
+                 workspace: Optional[Workspace] = None, out=None):
     """The budget from the draft alone, before the target runs (spec_draft_budget).
 
     draft [B, K, V] bf16/fp32, tokens [B, K] int32.  Either `budget` (N >= 0) or `cost`
-    ((cost_n, cost_t), N chosen by utility / cost).  Returns N (int32 [1]), depth [B] int32 and
-    the prefix confidences prod q_k(x_k) [B, K].
+    ((cost_n, cost_t), N chosen by utility / cost; float32 CUDA tensors are used as they are).
+    Returns N (int32 [1]), depth [B] int32 and the prefix confidences prod q_k(x_k) [B, K], in
+    `out` = (N, depth, conf) when given.
     """
     if draft.dim() != 3:
         raise ValueError("draft logits must be [B, K, V]")
@@ -336,9 +337,15 @@ def draft_budget(draft, tokens, temperature: float, budget: Optional[int] = None
     cn, ct, nc = _cost_table(cost, dev)
     if nc == 0 and (budget is None or budget < 0):
         raise ValueError("draft_budget needs budget >= 0 or a cost table")
-    n_out = torch.zeros(1, dtype=torch.int32, device=dev)
-    depth = torch.empty(B, dtype=torch.int32, device=dev)
-    conf = torch.empty(B, K, dtype=torch.float32, device=dev)
+    if out is not None:
+        n_out, depth, conf = out
+        _need(n_out, "out N", dtype=torch.int32, shape=(1,), device=dev)
+        _need(depth, "out depth", dtype=torch.int32, shape=(B,), device=dev)
+        _need(conf, "out conf", dtype=torch.float32, shape=(B, K), device=dev)
+    else:
+        n_out = torch.zeros(1, dtype=torch.int32, device=dev)
+        depth = torch.empty(B, dtype=torch.int32, device=dev)
+        conf = torch.empty(B, K, dtype=torch.float32, device=dev)
     ws = (workspace or default_workspace(stream))
     buf = ws.get(B, K, V, code, stream)
     _check(lib().spec_draft_budget(_ptr(draft), code, _ptr(tokens), B, K, V, float(temperature),
