@@ -45,12 +45,12 @@ struct UnitRec {
 enum : int32_t { kModeAlpha = 0, kModeFull = 1, kModeSingle = 2 };
 
 // Per-row mass table of the sampling kernel, written by every warp of every CTA of the unit's
-// cluster (floats):
-//   a[c * 8 + w]                       alpha partial of warp w of CTA c (sum min(p, q))
+// cluster for rows that may draw (full / single mode), floats:
 //   m[((c * itmax + it) * 8 + w) * 2]  (R, P): residual mass sum max(0, p - q) and mass sum p of
-//                                      item `it` of warp w of CTA c (full / single rows)
-// in vocabulary order (c, it, w).  The cut kernels sum alpha and draw from these.
-constexpr int kMassMaxSegments = 80;                     // CTA x item segments of a row (V * e / 8 KB + 16)
+//                                      item `it` of warp w of CTA c
+// in vocabulary order (c, it, w).  The cut kernels draw from these.  (The draft-side budget
+// reuses the region for its per-part row partials.)
+constexpr int kMassMaxSegments = 80;                     // CTA x item segments of a row
 constexpr int kMassRowFloats = kMassMaxSegments * 8 * 2;
 
 // Greedy path: per (request, position) two 64-bit argmax keys (target row, draft row), folded
