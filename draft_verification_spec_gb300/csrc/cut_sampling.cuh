@@ -93,7 +93,7 @@ __device__ __forceinline__ void cut_sampling(const BudgetParams& P, int b, int d
   const int ncta = P.ncta, itmax = P.itmax, nseg = ncta * itmax;
   const int esz = P.bf16 ? 2 : 4;
   const int IL = kSampItemBytes / esz, WS = kSampWarpBytes / esz, EPP = 16 / esz, PS = 32 * EPP;
-  const int nent = nseg * 8;
+  const int nent = nseg * kSampWarps;
   // the row's (R, P) entries in (CTA, item, warp) order, 0 where CTA c's slice has no item it;
   // lane l holds entries base + l*8 .. base + l*8 + 7 of a 256-entry chunk (one chunk for most rows)
   auto load_chunk = [&](int base, float2 (&m)[8]) {
@@ -102,7 +102,7 @@ __device__ __forceinline__ void cut_sampling(const BudgetParams& P, int b, int d
       const int e = base + lane * 8 + i;
       m[i] = make_float2(0.f, 0.f);
       if (e < nent) {
-        const int sg = e >> 3, c = sg / itmax, it = sg - c * itmax;
+        const int sg = e / kSampWarps, c = sg / itmax, it = sg - c * itmax;
         if (it * IL < min(P.slice, V - c * P.slice)) m[i] = __ldcg(reinterpret_cast<const float2*>(mrow) + e);
       }
     }
@@ -167,7 +167,7 @@ __device__ __forceinline__ void cut_sampling(const BudgetParams& P, int b, int d
   }
   int tok = -1;
   if (owner >= 0) {
-    const int sg = owner >> 3, w = owner & 7, c = sg / itmax, it = sg - c * itmax;
+    const int sg = owner / kSampWarps, w = owner % kSampWarps, c = sg / itmax, it = sg - c * itmax;
     const int nc = min(P.slice, V - c * P.slice);
     const int s0 = it * IL + w * WS;       // first logit of the segment in CTA c's slice
     const int v0 = c * P.slice + s0;       // ... in the row

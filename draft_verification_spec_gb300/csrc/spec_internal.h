@@ -46,12 +46,12 @@ enum : int32_t { kModeAlpha = 0, kModeFull = 1, kModeSingle = 2 };
 
 // Per-row mass table of the sampling kernel, written by every warp of every CTA of the unit's
 // cluster for rows that may draw (full / single mode), floats:
-//   m[((c * itmax + it) * 8 + w) * 2]  (R, P): residual mass sum max(0, p - q) and mass sum p of
+//   m[((c * itmax + it) * kSampWarps + w) * 2]  (R, P): residual mass sum max(0, p - q) and sum p of
 //                                      item `it` of warp w of CTA c
 // in vocabulary order (c, it, w).  The cut kernels draw from these.  (The draft-side budget
 // reuses the region for its per-part row partials.)
 constexpr int kMassMaxSegments = 80;                     // CTA x item segments of a row
-constexpr int kMassRowFloats = kMassMaxSegments * 8 * 2;
+constexpr int kMassRowFloats = kMassMaxSegments * kSampWarps * 2;
 
 // Greedy path: per (request, position) two 64-bit argmax keys (target row, draft row), folded
 // with atomicMax by the argmax kernel and cleared by the kernel that consumes them.
