@@ -10,17 +10,17 @@
 // sits between a copy and its use, and a wait is one cp.async.wait_group.
 //   pass 1, as the unit's asynchronous copies land (one commit group per item): per-lane online
 //     (max, sum of 2^((z - m) c)) of the target and draft rows -> warp maximum and rescaled warp
-//     sum -> exchange with st.async into every CTA of the cluster, completing on its mbarrier ->
-//     the row normalisers of p and q, merged in one fixed order so every warp of every CTA holds
-//     bitwise-identical values; p_k(x_k), q_k(x_k) and the accept test, exactly as the cut kernel
-//     evaluates them afterwards
+//     sum -> the CTA's partial, merged by warp 0 in warp order -> one st.async into every CTA of
+//     the cluster, completing on its mbarrier -> the row normalisers of p and q, merged in rank
+//     order by warp 0 of every CTA (bitwise-identical values everywhere); p_k(x_k), q_k(x_k) and
+//     the accept test, exactly as the cut kernel evaluates them afterwards
 //   pass 2, from shared memory: per logit p = 2^(z c - offt), q = 2^(z c - offd).  A pair that
 //     passes the test and needs no draw only needs alpha = sum 2^min(a, b) (one exp2 per logit
 //     pair); otherwise every warp writes its (item, warp) masses of r = max(0, p - q) and of p to
 //     the row's mass table.  As soon as a lane is done with an item, it copies its pieces of the
-//     next unit's item into the same bytes.  Every warp's alpha partial reaches rank 0 with the
-//     next exchange (the last unit's in an exchange of its own), and rank 0 writes the row's alpha,
-//     summed in (CTA, warp) order, to its record.
+//     next unit's item into the same bytes.  The CTA's alpha partial (its warps' in warp order)
+//     reaches rank 0 with the next exchange (the last unit's in an exchange of its own), and rank
+//     0 writes the row's alpha, summed in rank order, to its record.
 // The draws themselves are made by the chained cut kernel from the mass tables.  While a CTA
 // waits on its cluster's exchange, the other CTAs resident on its SM keep HBM busy.  A target row
 // that no draw needs is skipped entirely.  Rows that do not start on 16-byte boundaries are read
@@ -122,15 +122,15 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
   constexpr int IL = G::IL, WS = G::WS, PS = G::PS;
   constexpr int NWARP = kSampWarps;
   constexpr int IB = kSampItemBytes, WB = kSampWarpBytes;
-  constexpr int ENT = kMaxCluster * NWARP;         // exchange entries per row: (CTA c, warp w) at c*NWARP + w
-  constexpr int EPL = ENT / 32;
   constexpr int NQ = BF16 ? NWD : NWD / 2;         // logit pairs per lane per row per item
   constexpr uint32_t NEG = BF16 ? 0xff80ff80u : 0xff800000u;
 
   // the slab: warp w, item it, row r (0 target, 1 draft) at byte ((w * itmax + it) * 2 + r) * WB
   extern __shared__ __align__(128) uint8_t slab[];
-  __shared__ __align__(16) float4 mbox1[2][ENT];               // (m_t, s_t, m_d, s_d) per (CTA, warp)
-  __shared__ float abox[2][ENT];                               // rank 0: the previous unit's alpha partials
+  __shared__ __align__(16) float4 mbox1[2][kMaxCluster];       // (m_t, s_t, m_d, s_d) per CTA of the cluster
+  __shared__ float abox[2][kMaxCluster];                       // rank 0: the previous unit's alpha per CTA
+  __shared__ __align__(16) float4 part_sh[NWARP];              // this CTA's warp partials
+  __shared__ float apart_sh[NWARP];                            // this CTA's warp alpha partials
   __shared__ __align__(8) uint64_t x1_bar[2];
   __shared__ float norm_sh[2];                                 // offt, offd of the current unit
   __shared__ int mode_sh;
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
   const bool stats_only = (P.flags & F_STATS_ONLY) != 0;
   const bool all_pdraws = (P.flags & F_ALL_PDRAWS) != 0;
   const float c = P.c;
-  const int nent = static_cast<int>(C) * NWARP;
+  const int nc = static_cast<int>(C);                          // exchange entries per unit: one per CTA
   const int nunits = static_cast<int>(cid) < P.total_units
                          ? (P.total_units - static_cast<int>(cid) + static_cast<int>(ncl) - 1) / static_cast<int>(ncl)
                          : 0;
@@ -443,30 +443,27 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
       }
   }
 
-  // alpha of a pair: every warp's partial of unit i travels to rank 0 with the exchange of unit
-  // i + 1 (or a last exchange of its own), where warp 0 sums the partials in (CTA, warp) order
+  // alpha of a pair: each CTA's partial of unit i (its warps' partials summed in warp order)
+  // travels to rank 0 with the exchange of unit i + 1 (or a last exchange of its own), where warp 0
+  // sums the CTAs' partials in rank order
   bool has_prev = false;
   float prev_aw = 0.f;
   int prev_rec = 0;
   auto alpha_to_record = [&](int par) {
-    float s = 0.f;
-#pragma unroll
-    for (int q = 0; q < EPL; ++q) {
-      const int e = lane * EPL + q;
-      if (e < nent) s += abox[par][e];
-    }
-    s = warp_sum(s);
+    const float s = warp_sum(lane < nc ? abox[par][lane] : 0.f);
     if (lane == 0) P.recs[prev_rec].alpha = fminf(fmaxf(s, 0.f), 1.f);   // NaN -> 0
   };
+  // warp 0: the sum of the CTA's warp alpha partials in warp order
+  auto cta_alpha = [&]() { return warp_sum(lane < NWARP ? apart_sh[lane] : 0.f); };
 
   while (hasA) {
     const int apar = A.idx & 1;
     if (tid == 0)
-      mbar_arrive_tx(smem_addr(&x1_bar[apar]),
-                     static_cast<uint32_t>(nent) * (rank == 0 && has_prev ? 20u : 16u));
+      mbar_arrive_tx(smem_addr(&x1_bar[apar]), static_cast<uint32_t>(nc) * (rank == 0 && has_prev ? 20u : 16u));
 
-    // ---- pass 1, then the warp partials (warp maximum, every lane's sum rescaled to it) to every
-    // CTA of the cluster
+    // ---- pass 1, then the warp partials (warp maximum, every lane's sum rescaled to it), merged
+    // by warp 0 in warp order into the CTA's partial, which goes to every CTA of the cluster (with
+    // the previous unit's alpha partial to rank 0)
     float mt = ninf(), st = 0.f, md = ninf(), sd = 0.f;
     if (A.pair) pass1(std::true_type(), A, mt, st, md, sd);
     else pass1(std::false_type(), A, mt, st, md, sd);
@@ -475,13 +472,24 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
       const float rt = wt == ninf() ? 0.f : wt, rd = wd == ninf() ? 0.f : wd;
       st = warp_sum(st * ex2((mt - rt) * c));
       sd = warp_sum(sd * ex2((md - rd) * c));
-      if (lane < static_cast<int>(C)) {
-        const uint32_t dst = smem_addr(&mbox1[apar][rank * NWARP + warp]);
-        st_async_v4(peer_addr(dst, lane), wt, st, wd, sd, peer_addr(smem_addr(&x1_bar[apar]), lane));
+      if (lane == 0) {
+        part_sh[warp] = make_float4(wt, st, wd, sd);
+        apart_sh[warp] = prev_aw;
       }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const float4 v = lane < NWARP ? part_sh[lane] : make_float4(ninf(), 0.f, ninf(), 0.f);
+      const float Mt = warp_maxf(v.x), Md = warp_maxf(v.z);
+      const float rt = Mt == ninf() ? 0.f : Mt, rd = Md == ninf() ? 0.f : Md;
+      const float St = warp_sum(lane < NWARP ? v.y * ex2((v.x - rt) * c) : 0.f);
+      const float Sd = warp_sum(lane < NWARP ? v.w * ex2((v.z - rd) * c) : 0.f);
+      const float Ac = cta_alpha();
+      if (lane < nc)
+        st_async_v4(peer_addr(smem_addr(&mbox1[apar][rank]), lane), Mt, St, Md, Sd,
+                    peer_addr(smem_addr(&x1_bar[apar]), lane));
       if (has_prev && lane == 0)
-        st_async_f32(peer_addr(smem_addr(&abox[apar][rank * NWARP + warp]), 0), prev_aw,
-                     peer_addr(smem_addr(&x1_bar[apar]), 0));
+        st_async_f32(peer_addr(smem_addr(&abox[apar][rank]), 0), Ac, peer_addr(smem_addr(&x1_bar[apar]), 0));
     }
 
     // ---- the next unit (while the exchange completes), then the row normalisers and the accept
@@ -493,33 +501,11 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
     if (warp == 0) {
       if (lane == 0) wait_phase(smem_addr(&x1_bar[apar]), (A.idx >> 1) & 1);
       __syncwarp();
-      float Mt = ninf(), Md = ninf();
-#pragma unroll
-      for (int q = 0; q < EPL; ++q) {
-        const int e = lane * EPL + q;
-        if (e < nent) {
-          const float4 v = mbox1[apar][e];
-          Mt = fmaxf(Mt, v.x);
-          Md = fmaxf(Md, v.z);
-        }
-      }
-      Mt = warp_maxf(Mt);
-      Md = warp_maxf(Md);
-      float St = 0.f, Sd = 0.f;
-      {
-        const float rt = (Mt == ninf()) ? 0.f : Mt, rd = (Md == ninf()) ? 0.f : Md;
-#pragma unroll
-        for (int q = 0; q < EPL; ++q) {
-          const int e = lane * EPL + q;
-          if (e < nent) {
-            const float4 v = mbox1[apar][e];
-            St += v.y * ex2((v.x - rt) * c);
-            Sd += v.w * ex2((v.z - rd) * c);
-          }
-        }
-      }
-      St = warp_sum(St);
-      Sd = warp_sum(Sd);
+      const float4 v = lane < nc ? mbox1[apar][lane] : make_float4(ninf(), 0.f, ninf(), 0.f);
+      const float Mt = warp_maxf(v.x), Md = warp_maxf(v.z);
+      const float rt = (Mt == ninf()) ? 0.f : Mt, rd = (Md == ninf()) ? 0.f : Md;
+      const float St = warp_sum(lane < nc ? v.y * ex2((v.x - rt) * c) : 0.f);
+      const float Sd = warp_sum(lane < nc ? v.w * ex2((v.z - rd) * c) : 0.f);
       if (lane == 0) {
         // p_v = 2^(z c - offt), q_v = 2^(z c - offd): the normalisers folded into the exponent
         const float offt = (Mt == ninf() ? 0.f : Mt * c) + lg2f(St);
@@ -566,10 +552,14 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
     if (!hasN) {
       // the last unit's alpha partials, in an exchange of their own (only rank 0 receives and waits)
       const int i = A.idx + 1, par = i & 1;
-      if (rank == 0 && tid == 0) mbar_arrive_tx(smem_addr(&x1_bar[par]), static_cast<uint32_t>(nent) * 4u);
-      if (lane == 0)
-        st_async_f32(peer_addr(smem_addr(&abox[par][rank * NWARP + warp]), 0), prev_aw,
-                     peer_addr(smem_addr(&x1_bar[par]), 0));
+      if (rank == 0 && tid == 0) mbar_arrive_tx(smem_addr(&x1_bar[par]), static_cast<uint32_t>(nc) * 4u);
+      if (lane == 0) apart_sh[warp] = prev_aw;
+      __syncthreads();
+      if (warp == 0) {
+        const float Ac = cta_alpha();
+        if (lane == 0)
+          st_async_f32(peer_addr(smem_addr(&abox[par][rank]), 0), Ac, peer_addr(smem_addr(&x1_bar[par]), 0));
+      }
       if (rank == 0) {
         if (tid == 0) wait_phase(smem_addr(&x1_bar[par]), (i >> 1) & 1);
         __syncthreads();
