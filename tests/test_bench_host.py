@@ -89,3 +89,19 @@ def test_verified_tokens_is_the_budget_when_there_is_one():
     w = W.budget_sweep(4, V=1000)
     assert bench.verified_tokens(w) == 32
     assert bench.verified_tokens(W.greedy_mtp(B=2, V=1000)) == 6
+
+
+def test_draft_budget_configs_read_only_the_draft_rows():
+    """The draft-side budget configurations run on the budget sweep's draft rows alone: the entry
+    point, the algorithmic bytes (draft rows once, tokens, depth, confidences, N) and the cost
+    table (n from B to B(K+1), increasing cost)."""
+    w = W.budget_sweep(4, V=1000)
+    assert bench.call_kind(w, "draft_budget_B4") == ("draft", True)
+    assert bench.call_kind(w, "draft_budget_adaptive_B4") == ("draft_adaptive", True)
+    B, K, V = w.B, w.K, w.V
+    want = B * K * V * w.draft.element_size() + B * K * 4 + B * 4 + B * K * 4 + 4
+    assert bench.algorithmic_bytes(w, True, "draft") == want
+    assert bench.algorithmic_bytes(w, True, "draft_adaptive") == want
+    n, t = W.verify_cost_table(B, K)
+    assert n[0] == B and n[-1] == B * (K + 1) and all(a < b for a, b in zip(n, n[1:]))
+    assert all(a <= b for a, b in zip(t, t[1:]))
