@@ -59,13 +59,15 @@ __device__ __forceinline__ float cost_at(float n, const float* cn, const float* 
 
 // The budget N with the largest expected tokens per unit of verification cost: the first N
 // maximising (B + S(N)) / cost(B + N), S(N) the sum of the N largest prefix confidences.  Every
-// thread of the CTA calls it and gets the same N (the confidences are sorted in shared memory:
-// bitonic sort, descending; then one scan).
+// thread of the CTA calls it and gets the same N (the confidences are sorted in shared memory by
+// a bitonic network, descending -- exchange steps with strides of 32 and more through shared
+// memory with a barrier each, the shorter ones in registers, a warp per 32 consecutive elements
+// exchanging by shuffle -- then one scan).
 __device__ int choose_budget(const BudgetParams& P, const float* conf, float* sb, float* cn, float* ct,
                              float* red_u, int* red_n, int* n_out) {
   const int BK = P.B * P.K, tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
   const int nw = nt >> 5;
-  int n2 = 1;
+  int n2 = 32;
   while (n2 < BK) n2 <<= 1;
   for (int i = tid; i < n2; i += nt) sb[i] = i < BK ? conf[i] : -1.f;
   for (int i = tid; i < P.n_cost; i += nt) {
@@ -73,8 +75,23 @@ __device__ int choose_budget(const BudgetParams& P, const float* conf, float* sb
     ct[i] = P.cost_t[i];
   }
   __syncthreads();
-  for (int k = 2; k <= n2; k <<= 1)
-    for (int j = k >> 1; j > 0; j >>= 1) {
+  // the exchange steps of stages kmin .. kmax with strides below 32, in registers
+  auto warp_steps = [&](int kmin, int kmax) {
+    for (int base = warp * 32; base < n2; base += nw * 32) {
+      const int i = base + lane;
+      float a = sb[i];
+      for (int k = kmin; k <= kmax; k <<= 1)
+        for (int j = min(k >> 1, 16); j > 0; j >>= 1) {
+          const float bv = __shfl_xor_sync(0xffffffffu, a, j);
+          a = (((i & j) == 0) == ((i & k) == 0)) ? fmaxf(a, bv) : fminf(a, bv);   // descending blocks keep the larger first
+        }
+      sb[i] = a;
+    }
+    __syncthreads();
+  };
+  warp_steps(2, 32);
+  for (int k = 64; k <= n2; k <<= 1) {
+    for (int j = k >> 1; j >= 32; j >>= 1) {
       for (int i = tid; i < n2; i += nt) {
         const int l = i ^ j;
         if (l > i) {
@@ -87,6 +104,8 @@ __device__ int choose_budget(const BudgetParams& P, const float* conf, float* sb
       }
       __syncthreads();
     }
+    warp_steps(k, k);
+  }
   // S(N): each thread sums a contiguous run of the sorted values; a scan of the runs' totals
   const int per = (BK + nt - 1) / nt;
   const int i0 = min(BK, tid * per), i1 = min(BK, i0 + per);
@@ -186,7 +205,7 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid
   __syncthreads();
   int Nsel = P.N;
   if (P.n_cost > 0) {
-    int n2 = 1;
+    int n2 = 32;
     while (n2 < B * K) n2 <<= 1;
     float* const sb = conf + 2 * B * K;
     float* const cn = sb + n2;
@@ -275,7 +294,7 @@ cudaError_t launch_budget_cut(const BudgetParams& p, cudaStream_t stream, bool p
   const int grid = (p.greedy && p.keys) ? 1 : (p.B + per - 1) / per;
   size_t smem = static_cast<size_t>(p.B) * p.K * sizeof(float) * 2;
   if (p.n_cost > 0) {
-    size_t n2 = 1;
+    size_t n2 = 32;
     while (n2 < static_cast<size_t>(p.B) * p.K) n2 <<= 1;
     smem += (n2 + 2 * kBudgetMaxCost + 64) * sizeof(float);
   }
