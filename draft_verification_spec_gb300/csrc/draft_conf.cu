@@ -29,6 +29,9 @@ __global__ void __launch_bounds__(kDraftStatsThreads) draft_stats_kernel(const _
   __shared__ float sm_m[NW], sm_s[NW];
   __shared__ unsigned sm_i[NW];
 
+  // the budget kernel chained after this one may start (it reads only the caller's inputs
+  // before it waits for this grid)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int part = blockIdx.x, row = blockIdx.y;
   const int lo = part * P.part_len, hi = min(P.V, lo + P.part_len);
