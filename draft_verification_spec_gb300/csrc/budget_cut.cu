@@ -292,12 +292,14 @@ __host__ __device__ constexpr int budget_values_per_thread(int n2) {
 // stored position-major ([K][B]), so lanes that read different requests at one position -- or at
 // different positions -- hit different banks.
 __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid_constant__ BudgetParams P) {
-  // [K, B] prefix confidences, [K, B] per-position confidences, then the selection's exchange
-  // area (2 n2 floats) and its sorted confidences (n2 floats)
+  // [K, B] prefix confidences, [K, B] per-position confidences, [K, B] accept-test failures (one
+  // byte each, sampling path), then the selection's exchange area (2 n2 floats) and its sorted
+  // confidences (n2 floats)
   extern __shared__ __align__(16) float conf[];
   __shared__ BudgetShared sh;
   const int B = P.B, K = P.K, BK = B * K;
   float* const alpha_s = conf + BK;
+  uint8_t* const rej_s = reinterpret_cast<uint8_t*>(conf + 2 * BK);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   auto load_costs = [&]() {
     for (int i = threadIdx.x; i < P.n_cost; i += blockDim.x) {
@@ -345,9 +347,13 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid
         alpha_s[k * B + b] = draft_q(P, r, draft_pick(P, r));
       }
     } else {
+      // each row's alpha, and the outcome of its accept test as the row kernel evaluated it (the
+      // cuts read it from shared memory): the record's second 16-byte word, (mode, alpha, rej, -)
       for (int r = threadIdx.x; r < BK; r += blockDim.x) {
         const int b = r / K, k = r - b * K;
-        alpha_s[k * B + b] = alpha_of_row(P, b, k);
+        const float4 w = __ldcg(reinterpret_cast<const float4*>(P.recs + static_cast<size_t>(b) * P.U + k) + 1);
+        alpha_s[k * B + b] = w.y;
+        rej_s[k * B + b] = __float_as_int(w.z) != 0 ? 1 : 0;
       }
     }
     __syncthreads();
@@ -366,7 +372,7 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid
   if (P.n_cost > 0 || (P.N > 0 && P.N < BK)) {
     int n2 = 32;
     while (n2 < BK) n2 <<= 1;
-    float* const xb = conf + 2 * BK;
+    float* const xb = conf + 2 * BK + (BK + 3) / 4;
     switch (budget_values_per_thread(n2)) {
       case 1: cut = budget_cut_of<1>(P, conf, n2, xb, sh, &Nsel); break;
       case 2: cut = budget_cut_of<2>(P, conf, n2, xb, sh, &Nsel); break;
@@ -390,7 +396,7 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid
         cut_request(b, d, P.stats_only != 0, P.keys, P.draft_keys != 0, false, P.U, K, P.V, P.tokens,
                     P.out_tokens, P.out_accepted, P.out_alpha, P.out_cum, P.out_E, P.status, lane);
       else
-        cut_sampling(P, b, d, lane, true, lane < K ? alpha_s[lane * B + b] : 0.f);
+        cut_sampling(P, b, d, lane, true, lane < K ? alpha_s[lane * B + b] : 0.f, rej_s);
     }
   }
   if (P.greedy && P.keys) {   // every warp of the (single) CTA is done with the keys: clear them
@@ -437,7 +443,7 @@ cudaError_t launch_budget_cut(const BudgetParams& p, cudaStream_t stream, bool p
   // CTA builds the table and a warp cuts one request
   const int grid = (p.greedy && p.keys) ? 1 : (p.B + per - 1) / per;
   const int BK = p.B * p.K;
-  size_t smem = static_cast<size_t>(BK) * sizeof(float) * 2;
+  size_t smem = static_cast<size_t>(BK) * sizeof(float) * 2 + static_cast<size_t>((BK + 3) / 4) * sizeof(float);
   if (p.n_cost > 0 || (p.N > 0 && p.N < BK)) {   // the selection sorts: its exchange area
     int n2 = 32;
     while (n2 < BK) n2 <<= 1;

@@ -61,9 +61,10 @@ __device__ __forceinline__ float alpha_row_warp(const BudgetParams& P, int b, in
 }
 
 // The cut of request b at verified depth d (lane k <-> position k).  alpha_k may be given
-// (alpha_given, lane k's value), as the budget kernel already computed it.
+// (alpha_given, lane k's value), and so may the accept test of every position (rej_tab: the [K, B]
+// table of positions whose test fails, 1 byte each), as the budget kernel already computed them.
 __device__ __forceinline__ void cut_sampling(const BudgetParams& P, int b, int d, int lane, bool alpha_given = false,
-                                             float alpha_lane = 0.f) {
+                                             float alpha_lane = 0.f, const uint8_t* rej_tab = nullptr) {
   const int K = P.K, U = P.U, V = P.V;
   const UnitRec* rb = P.recs + static_cast<size_t>(b) * U;
   const float a = alpha_given ? alpha_lane : alpha_row_warp(P, b, lane);
@@ -76,9 +77,10 @@ __device__ __forceinline__ void cut_sampling(const BudgetParams& P, int b, int d
   int x = -1;
   if (lane < d) {
     x = P.tokens[static_cast<size_t>(b) * K + lane];
-    if (x < 0 || x >= V) {
+    if (rej_tab) {
+      ok = rej_tab[lane * P.B + b] == 0;
+    } else if (x < 0 || x >= V) {
       ok = false;
-      atomicOr(P.status, kStatusTokenRange);
     } else {
       const float u = P.uniforms[static_cast<size_t>(b) * (K + 1) + lane];
       ok = u * __ldcg(&rb[lane].qx) < __ldcg(&rb[lane].px);
@@ -276,6 +278,7 @@ __device__ __forceinline__ void cut_sampling(const BudgetParams& P, int b, int d
     es = __shfl_sync(0xffffffffu, es, l);
     tok = v0 + js * PS + l * EPP + es;
   }
+  if (lane < d && (x < 0 || x >= V)) atomicOr(P.status, kStatusTokenRange);   // (off the path to the draw)
   int32_t* ot = P.out_tokens + static_cast<size_t>(b) * (K + 1);
   for (int i = lane; i <= K; i += 32) ot[i] = (i < n) ? x : (i == n ? tok : -1);
   if (lane == 0) P.out_accepted[b] = n;

@@ -577,6 +577,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
           r->offt = offt;
           r->offd = offd;
           r->mode = mode;
+          r->rej = rejects ? 1 : 0;
         }
       }
     }

@@ -40,8 +40,11 @@ struct UnitRec {
   float offt, offd;  // p_v = 2^(z_T[v] c - offt), q_v = 2^(z_D[v] c - offd)
   int32_t mode;      // pass-2 work done: kModeAlpha, kModeFull or kModeSingle
   float alpha;       // sum_v min(p_v, q_v) of a pair, clamped to [0, 1] (written after the next exchange)
-  int32_t pad1, pad2;
+  int32_t rej;       // 1: the accept test u_k q_k(x_k) < p_k(x_k) fails at this position (k < K)
+  int32_t pad;
 };
+static_assert(sizeof(UnitRec) == 32 && offsetof(UnitRec, alpha) == 20 && offsetof(UnitRec, rej) == 24,
+              "the budget kernel reads (mode, alpha, rej) as the record's second 16-byte word");
 enum : int32_t { kModeAlpha = 0, kModeFull = 1, kModeSingle = 2 };
 
 // Per-row mass table of the sampling kernel, written by every warp of every CTA of the unit's
