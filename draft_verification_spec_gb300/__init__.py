@@ -138,21 +138,18 @@ class Tuning:
     """Per-call test and tuning knobs (spec_tuning_t); the defaults leave every choice to the library.
 
     wait_limit_us: 0 default (200 ms), > 0 a limit, < 0 every bounded device wait gives up at once.
-    cluster: sampling kernel CTAs per row (0 automatic).  resident_items: items of each row the
-    sampling kernel keeps in shared memory between its passes, the rest read again (0 automatic).
-    greedy_variant: bit 1 separate cut kernel,
+    cluster: sampling kernel CTAs per row (0 automatic).  greedy_variant: bit 1 separate cut kernel,
     bit 2 every resident CTA slot.  split_event: a torch.cuda.Event recorded between the row kernel
     and the kernel chained after it.  After the call, ``plan`` holds the launched plan.
     """
 
     KEYS = ("threads", "cluster", "clusters", "max_clusters", "slice", "items", "smem_bytes", "flags")
 
-    def __init__(self, wait_limit_us: int = 0, cluster: int = 0, greedy_variant: int = 0, split_event=None,
-                 resident_items: int = 0):
+    def __init__(self, wait_limit_us: int = 0, cluster: int = 0, greedy_variant: int = 0, split_event=None):
         self._plan = (ctypes.c_int32 * 8)()
         ev = None if split_event is None else ctypes.c_void_p(split_event.cuda_event)
         self._c = _lib.SpecTuning(int(wait_limit_us), int(cluster), int(greedy_variant),
-                                  ctypes.cast(self._plan, ctypes.c_void_p), ev, int(resident_items))
+                                  ctypes.cast(self._plan, ctypes.c_void_p), ev)
 
     @property
     def plan(self) -> dict:

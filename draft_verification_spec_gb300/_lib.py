@@ -18,7 +18,7 @@ c_longlong = ctypes.c_longlong
 class SpecTuning(ctypes.Structure):
     """spec_tuning_t: per-call test and tuning knobs (all zero = defaults)."""
     _fields_ = [("wait_limit_us", c_longlong), ("cluster", c_int), ("greedy_variant", c_int),
-                ("plan_out", c_void_p), ("split_event", c_void_p), ("resident_items", c_int)]
+                ("plan_out", c_void_p), ("split_event", c_void_p)]
 
 # name -> (restype, argtypes), mirroring include/spec_verify.h
 SIGNATURES = {

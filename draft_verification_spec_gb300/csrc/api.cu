@@ -4,7 +4,6 @@
 // The library keeps no mutable state between calls except two per-device caches (kernel
 // attributes set, occupancy answers), guarded by a mutex.  Tuning and test knobs travel with
 // the call (spec_tuning_t), never through process-wide settings.
-#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <map>
@@ -69,7 +68,6 @@ struct Knobs {
   long long wait_ns = kDefaultWaitNs;
   int cluster = 0;
   int variant = 0;
-  int resident = 0;
   int32_t* plan_out = nullptr;
   cudaEvent_t split = nullptr;
 };
@@ -80,7 +78,6 @@ Knobs knobs_of(const spec_tuning_t* t) {
   if (t->wait_limit_us < 0) k.wait_ns = 0;
   k.cluster = t->cluster;
   k.variant = t->greedy_variant & 7;
-  k.resident = t->resident_items > 0 ? t->resident_items : 0;
   k.plan_out = t->plan_out;
   k.split = static_cast<cudaEvent_t>(t->split_event);
   return k;
@@ -96,9 +93,9 @@ std::map<std::tuple<int, const void*, int, int>, int> g_maxc;
 std::map<int, std::tuple<int, int, size_t>> g_dev;   // SMs, L2 bytes
 // chosen sampling plan per call shape
 struct PlanChoice {
-  int cluster, nclusters, maxc, nres;
+  int cluster, nclusters, maxc;
 };
-std::map<std::tuple<int, const void*, int, int, int, int, int, int>, PlanChoice> g_plans;
+std::map<std::tuple<int, const void*, int, int, int, int, int>, PlanChoice> g_plans;
 
 cudaError_t device_info(int dev, int* sms, size_t* l2) {
   {
@@ -176,9 +173,7 @@ struct RowPlan {
 // Estimated duration (seconds) of the sampling kernel with clusters of C CTAs: units go
 // round-robin to the clusters (pairs first); a CTA reads its slice of a unit's rows at its share
 // of the HBM bandwidth (bw_total over all CTAs, at most bw_cta each) and every step pays a fixed
-// cost t_step for the cluster exchange and the normalisers.  (A slice streamed past its first
-// item is read a second time from L2, which this model leaves out: where the streamed bytes in
-// flight fit in L2 the timings follow it.)
+// cost t_step for the cluster exchange and the normalisers.
 double plan_cost(int C, int ncl, int npairs, int nsingle, double row_bytes, double bw_total, double bw_cta,
                  double t_step) {
   const int units = npairs + nsingle;
@@ -193,9 +188,8 @@ double plan_cost(int C, int ncl, int npairs, int nsingle, double row_bytes, doub
   }
   return worst;
 }
-// Fitted to timings of the V = 128000 bf16 verification configurations on a GB300 (B = 4 .. 64,
-// chain and block calls, every cluster size, slabs resident and streamed).
-constexpr double kPlanBw = 6.0e12, kPlanBwCta = 1.5e10, kPlanStep = 2.0e-6;
+// Fitted to timings of the verification configurations on a GB300.
+constexpr double kPlanBw = 6.5e12, kPlanBwCta = 2.5e10, kPlanStep = 1.5e-6;
 
 spec_status_t plan_rows(const void* target, const void* draft, int dtype, int B, int K, int V, float T,
                         bool need_draft, bool stats_only, const Knobs& kn, RowPlan* plan) {
@@ -213,46 +207,29 @@ spec_status_t plan_rows(const void* target, const void* draft, int dtype, int B,
   const int item_logits = kItemBytes / esz;
   auto slice_of = [&](int C) { return static_cast<int>(align_up((V + C - 1) / C, sv::kChunk)); };
   auto items_of = [&](int C) { return (slice_of(C) + item_logits - 1) / item_logits; };
-  PlanChoice best = {0, 0, 0, 0};
-  const auto key = std::make_tuple(dev, fn, B, K, V, static_cast<int>(need_draft) | (stats_only ? 2 : 0), kn.cluster,
-                                   kn.resident);
+  PlanChoice best = {0, 0, 0};
+  const auto key = std::make_tuple(dev, fn, B, K, V, static_cast<int>(need_draft) | (stats_only ? 2 : 0), kn.cluster);
   {
     std::lock_guard<std::mutex> lk(g_mu);
     auto it = g_plans.find(key);
     if (it != g_plans.end()) best = it->second;
   }
   if (best.cluster == 0) {
-    // among the cluster sizes whose slice fits the slab (or streams), the cheapest estimated schedule
-    int sms = 0;
-    size_t l2 = 0;
-    if (device_info(dev, &sms, &l2) != cudaSuccess) return SPEC_ERR_CUDA;
+    // among the cluster sizes whose slice fits the slab, the cheapest estimated schedule
     double best_cost = 1e300;
     for (int C = 1; C <= sv::kMaxCluster; C *= 2) {
       if (kn.cluster && C != kn.cluster) continue;
       const int itmax = items_of(C);
-      if (C * itmax > sv::kMassMaxSegments) continue;
-      // the slab keeps every item of the slice when they fit (or the first resident_items of each
-      // row); otherwise rows on 16-byte boundaries keep their first item and stream the others,
-      // which are read a second time from L2 in pass 2
-      int nres = kn.resident ? std::min(itmax, kn.resident) : itmax;
-      if (!kn.resident && nres > sv::kSampMaxItems && aligned) nres = 1;
-      if (nres > sv::kSampMaxItems) continue;
+      if (itmax > sv::kSampMaxItems || C * itmax > sv::kMassMaxSegments) continue;
       int maxc = 0;
-      if (max_clusters(dev, fn, sv::kSampMaxSlabBytes, C, sv::samp_slab_bytes(nres), &maxc) != cudaSuccess)
+      if (max_clusters(dev, fn, sv::kSampMaxSlabBytes, C, sv::samp_slab_bytes(itmax), &maxc) != cudaSuccess)
         return SPEC_ERR_CUDA;
       if (maxc < 1) continue;
       const int ncl = units < maxc ? units : maxc;
-      // a streamed plan only where every cluster walks at least 4 units, and the streamed bytes that
-      // wait in L2 for their second read fit there (with fewer units per cluster the lines it keeps
-      // in L2 cost the chained cut more than the smaller clusters gain)
-      if (nres < itmax && !kn.resident && !kn.cluster) {
-        const double streamed = static_cast<double>(ncl) * C * (itmax - nres) * sv::kSampItemBytes * 2.0;
-        if (units < 4 * ncl || streamed > static_cast<double>(l2)) continue;
-      }
       const double cost = plan_cost(C, ncl, npairs, nsingle, row_bytes, kPlanBw, kPlanBwCta, kPlanStep);
       if (best.cluster == 0 || cost < best_cost * 0.97) {
         best_cost = cost;
-        best = {C, ncl, maxc, nres};
+        best = {C, ncl, maxc};
       }
     }
     if (best.cluster == 0) return SPEC_ERR_UNSUPPORTED;
@@ -265,7 +242,7 @@ spec_status_t plan_rows(const void* target, const void* draft, int dtype, int B,
   plan->cluster = best.cluster;
   plan->nclusters = best.nclusters;
   plan->maxc = best.maxc;
-  plan->smem = sv::samp_slab_bytes(best.nres);
+  plan->smem = sv::samp_slab_bytes(itmax);
   RowParams& p = plan->p;
   std::memset(&p, 0, sizeof(p));
   p.target = target;
@@ -277,7 +254,6 @@ spec_status_t plan_rows(const void* target, const void* draft, int dtype, int B,
   p.total_units = units;
   p.slice = slice;
   p.itmax = itmax;
-  p.nres = best.nres;
   p.flags = (need_draft ? sv::F_NEED_DRAFT : 0) | (stats_only ? sv::F_STATS_ONLY : 0) |
             (aligned ? sv::F_ALIGNED : 0);
   p.c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));

@@ -1,8 +1,7 @@
 // The small kernels chained after the row kernel:
 //  * cut_kernel: the serial first-rejection cut of each request (one warp per request);
 //  * budget_cut_kernel: the batch-level budget -- the global top-N of prefix confidences
-//    prod_{k<=m} alpha_k, prefix-closed per request, found by one sort of the B K confidences -- then
-//    the cut at the chosen depths.
+//    prod_{k<=m} alpha_k, prefix-closed per request -- then the cut at the chosen depths.
 // Both wait (griddepcontrol.wait) for the preceding kernel before they read its results, so they
 // may be scheduled while it drains.
 #include "argmax_kernel.cuh"
@@ -13,6 +12,11 @@ namespace sv {
 
 constexpr int kBudgetThreads = 512;
 constexpr int kCutThreads = 128;
+
+// key (c2, m2, b2) precedes key (c, m, b): c descending, then m ascending, then b ascending
+__device__ __forceinline__ bool precedes(float c2, int m2, int b2, float c, int m, int b) {
+  return c2 > c || (c2 == c && (m2 < m || (m2 == m && b2 < b)));
+}
 
 __device__ __forceinline__ float alpha_of(const BudgetParams& P, int b, int k) {
   if (P.alpha_in) return P.alpha_in[static_cast<size_t>(b) * P.K + k];
@@ -134,22 +138,13 @@ __device__ void sort_desc(float (&v)[E], int n2, int ts, float* xb) {
   }
 }
 
-// Shared scratch of the selection: the cost table, scan and reduction slots, the results.
+// Shared scratch of the choice of N: the cost table, scan and reduction slots, the result.
 struct BudgetShared {
   float cn[kBudgetMaxCost], ct[kBudgetMaxCost];
   float run[32], offset[32], best_u[32];
-  int best_n[32], ties[32], tie_off[32], above[32];
-  int n, above_all, r_last;
+  int best_n[32];
+  int n;
 };
-
-__device__ __forceinline__ int warp_incl_scan_int(int v, int lane) {
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += t;
-  }
-  return v;
-}
 
 // The budget N with the largest expected tokens per unit of verification cost: the first N
 // maximising (B + S(N)) / cost(B + N), S(N) the sum of the N largest prefix confidences, from the
@@ -211,22 +206,11 @@ __device__ int choose_budget(const BudgetParams& P, const float* srt, BudgetShar
   return sh.n;
 }
 
-// The last key the budget takes, in its order (c descending, then m ascending, then b ascending,
-// i.e. r = m B + b ascending): key (b, m) is taken when c(b, m) > c_last, or c(b, m) == c_last and
-// m B + b <= r_last.
-struct BudgetCut {
-  float c_last;
-  int r_last;
-};
-
-// The cut of the first N keys of the [K, B] table `conf` -- N the caller's, or the utility / cost
-// choice: all keys for N >= B K, none for N <= 0.  c_last is the N-th largest confidence (one
-// sort); of the ties at c_last, the first N - #{c > c_last} in increasing r are taken (one block
-// count and scan).  Writes N to *n_out.
+// The utility / cost choice of N over the [K, B] table `conf`: the confidences sorted (one
+// bitonic sort by the first n2 / E threads), then S(N) and the first maximum of U(N).
 template <int E>
-__device__ BudgetCut budget_cut_of(const BudgetParams& P, const float* conf, int n2, float* xb, BudgetShared& sh,
-                                   int* n_out) {
-  const int BK = P.B * P.K, tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+__device__ int adaptive_n(const BudgetParams& P, const float* conf, int n2, float* xb, BudgetShared& sh) {
+  const int BK = P.B * P.K, tid = threadIdx.x;
   const int ts = n2 / E;
   float* const srt = xb + 2 * n2;   // the sorted confidences, descending
   if (tid < ts) {
@@ -241,47 +225,10 @@ __device__ BudgetCut budget_cut_of(const BudgetParams& P, const float* conf, int
     for (int e = 0; e < E; ++e) srt[tid * E + e] = v[e];
   }
   __syncthreads();
-  const int N = P.n_cost > 0 ? choose_budget(P, srt, sh) : P.N;
-  *n_out = N;
-  if (N <= 0) return BudgetCut{2.f, -1};
-  if (N >= BK) return BudgetCut{-1.f, -1};
-  const float cl = srt[N - 1];
-  // each thread counts a contiguous run of positions: above c_last, and ties with it
-  const int per = (BK + nt - 1) / nt;
-  const int r0 = min(BK, tid * per), r1 = min(BK, r0 + per);
-  int above = 0, ties = 0;
-  for (int r = r0; r < r1; ++r) {
-    const float c = conf[r];
-    above += c > cl;
-    ties += c == cl;
-  }
-  const int ties_incl = warp_incl_scan_int(ties, lane);
-  const int above_w = warp_sum_int(above);
-  if (lane == 31) sh.ties[warp] = ties_incl;
-  if (lane == 0) sh.above[warp] = above_w;
-  __syncthreads();
-  if (warp == 0) {
-    const int t = lane < nw ? sh.ties[lane] : 0;
-    const int ti = warp_incl_scan_int(t, lane);
-    if (lane < nw) sh.tie_off[lane] = ti - t;
-    const int a = warp_sum_int(lane < nw ? sh.above[lane] : 0);
-    if (lane == 0) sh.above_all = a;
-  }
-  __syncthreads();
-  const int want = N - sh.above_all;   // ties taken: at least 1, at most the ties there are
-  int seen = sh.tie_off[warp] + ties_incl - ties;
-  if (seen < want && seen + ties >= want) {
-    for (int r = r0; r < r1; ++r)
-      if (conf[r] == cl && ++seen == want) {
-        sh.r_last = r;
-        break;
-      }
-  }
-  __syncthreads();
-  return BudgetCut{cl, sh.r_last};
+  return choose_budget(P, srt, sh);
 }
 
-// Values per sorting thread of the selection: n2 / 256 within [1, 16] (at most 256 sorting threads
+// Values per sorting thread of the choice of N: n2 / 256 within [1, 16] (at most 256 sorting threads
 // up to n2 = 4096; fewer threads with more values each issue fewer instructions a step).
 __host__ __device__ constexpr int budget_values_per_thread(int n2) {
   return n2 <= 256 ? 1 : (n2 / 256 > 16 ? 16 : n2 / 256);
@@ -293,8 +240,8 @@ __host__ __device__ constexpr int budget_values_per_thread(int n2) {
 // different positions -- hit different banks.
 __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid_constant__ BudgetParams P) {
   // [K, B] prefix confidences, [K, B] per-position confidences, [K, B] accept-test failures (one
-  // byte each, sampling path), then the selection's exchange area (2 n2 floats) and its sorted
-  // confidences (n2 floats)
+  // byte each, sampling path), then for the choice of N the sort's exchange area (2 n2 floats) and
+  // the sorted confidences (n2 floats)
   extern __shared__ __align__(16) float conf[];
   __shared__ BudgetShared sh;
   const int B = P.B, K = P.K, BK = B * K;
@@ -366,28 +313,43 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid
     }
   }
   __syncthreads();
-  // the selection: the first N keys in the budget order
   int Nsel = P.N;
-  BudgetCut cut = P.N <= 0 ? BudgetCut{2.f, -1} : BudgetCut{-1.f, -1};
-  if (P.n_cost > 0 || (P.N > 0 && P.N < BK)) {
+  if (P.n_cost > 0) {
     int n2 = 32;
     while (n2 < BK) n2 <<= 1;
     float* const xb = conf + 2 * BK + (BK + 3) / 4;
     switch (budget_values_per_thread(n2)) {
-      case 1: cut = budget_cut_of<1>(P, conf, n2, xb, sh, &Nsel); break;
-      case 2: cut = budget_cut_of<2>(P, conf, n2, xb, sh, &Nsel); break;
-      case 4: cut = budget_cut_of<4>(P, conf, n2, xb, sh, &Nsel); break;
-      case 8: cut = budget_cut_of<8>(P, conf, n2, xb, sh, &Nsel); break;
-      default: cut = budget_cut_of<16>(P, conf, n2, xb, sh, &Nsel); break;
+      case 1: Nsel = adaptive_n<1>(P, conf, n2, xb, sh); break;
+      case 2: Nsel = adaptive_n<2>(P, conf, n2, xb, sh); break;
+      case 4: Nsel = adaptive_n<4>(P, conf, n2, xb, sh); break;
+      case 8: Nsel = adaptive_n<8>(P, conf, n2, xb, sh); break;
+      default: Nsel = adaptive_n<16>(P, conf, n2, xb, sh); break;
     }
-    if (P.n_cost > 0 && blockIdx.x == 0 && threadIdx.x == 0 && P.out_N) *P.out_N = Nsel;
+    if (blockIdx.x == 0 && threadIdx.x == 0 && P.out_N) *P.out_N = Nsel;
   }
   for (int b = blockIdx.x * nw + warp; b < B; b += gridDim.x * nw) {
-    // d_b: the positions taken, a prefix of m (c never grows with m, and among ties the smaller
-    // m comes first)
-    const float cm = lane < K ? conf[lane * B + b] : -1.f;
-    const bool sel = lane < K && (cm > cut.c_last || (cm == cut.c_last && lane * B + b <= cut.r_last));
-    const int d = __popc(__ballot_sync(0xffffffffu, sel));
+    // rank of key (b, m): within each request b' the keys that precede it form a prefix (conf
+    // is non-increasing in m'), found by binary search; lanes split the requests
+    auto rank_of = [&](int m) {
+      const float cv = conf[m * B + b];
+      int cnt = 0;
+      for (int bp = lane; bp < B; bp += 32) {
+        int lo = 0, hi = K;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (precedes(conf[mid * B + bp], mid, bp, cv, m, b)) lo = mid + 1; else hi = mid;
+        }
+        cnt += lo;
+      }
+      return warp_sum_int(cnt);
+    };
+    // d_b = the number of m whose key ranks below N (a prefix of m)
+    int lo = 0, hi = K;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (rank_of(mid) < Nsel) lo = mid + 1; else hi = mid;
+    }
+    const int d = lo;
     if (P.out_depth && lane == 0) P.out_depth[b] = d;
     if (P.out_conf)
       for (int k = lane; k < K; k += 32) P.out_conf[static_cast<size_t>(b) * K + k] = conf[k * B + b];
@@ -444,7 +406,7 @@ cudaError_t launch_budget_cut(const BudgetParams& p, cudaStream_t stream, bool p
   const int grid = (p.greedy && p.keys) ? 1 : (p.B + per - 1) / per;
   const int BK = p.B * p.K;
   size_t smem = static_cast<size_t>(BK) * sizeof(float) * 2 + static_cast<size_t>((BK + 3) / 4) * sizeof(float);
-  if (p.n_cost > 0 || (p.N > 0 && p.N < BK)) {   // the selection sorts: its exchange area
+  if (p.n_cost > 0) {   // the choice of N sorts: its exchange area and the sorted values
     int n2 = 32;
     while (n2 < BK) n2 <<= 1;
     smem += 3 * static_cast<size_t>(n2) * sizeof(float);

@@ -69,17 +69,6 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
-__device__ __forceinline__ uint64_t l2_evict_last_policy() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-// 16-byte read-only load into registers with an L2 eviction policy.
-__device__ __forceinline__ void ldg16(uint32_t* w, const uint8_t* src, uint64_t policy) {
-  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-               : "l"(src), "l"(policy));
-}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
@@ -136,7 +125,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
   constexpr int NQ = BF16 ? NWD : NWD / 2;         // logit pairs per lane per row per item
   constexpr uint32_t NEG = BF16 ? 0xff80ff80u : 0xff800000u;
 
-  // the slab: warp w, resident item it, row r (0 target, 1 draft) at byte ((w * nres + it) * 2 + r) * WB
+  // the slab: warp w, item it, row r (0 target, 1 draft) at byte ((w * itmax + it) * 2 + r) * WB
   extern __shared__ __align__(128) uint8_t slab[];
   __shared__ __align__(16) float4 mbox1[2][kMaxCluster];       // (m_t, s_t, m_d, s_d) per CTA of the cluster
   __shared__ float abox[2][kMaxCluster];                       // rank 0: the previous unit's alpha per CTA
@@ -155,7 +144,6 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
   const int lo = static_cast<int>(rank) * P.slice;
   const int n = max(0, min(P.slice, V - lo));                  // this CTA's slice length
   const int nitems = (n + IL - 1) / IL;
-  const int nres = min(P.nres, nitems);                        // items of each row kept in the slab
   const bool need_draft = (P.flags & F_NEED_DRAFT) != 0;
   const bool stats_only = (P.flags & F_STATS_ONLY) != 0;
   const bool all_pdraws = (P.flags & F_ALL_PDRAWS) != 0;
@@ -171,7 +159,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
   const int el = warp * WS + lane * EPP;
   // logits of this warp's part of the last item that lie inside the slice
   const int last_nval = nitems > 0 ? min(WS, max(0, n - (nitems - 1) * IL - warp * WS)) : 0;
-  const uint32_t slab_l = smem_addr(slab) + static_cast<uint32_t>(warp * P.nres * 2 * WB + lane * 16);
+  const uint32_t slab_l = smem_addr(slab) + static_cast<uint32_t>(warp * itmax * 2 * WB + lane * 16);
   auto slot = [&](int it, int r) -> uint32_t { return slab_l + static_cast<uint32_t>((it * 2 + r) * WB); };
 
   // unit u -> (b, k): the pairs first (b-major), then the target rows k = K (or, without draft
@@ -205,7 +193,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
   }
   mbar_fence_init();
   // pieces of the last item past the slice end are never copied: they hold -inf for good
-  if (nitems > 0 && nitems <= P.nres) {
+  if (nitems > 0) {
     const uint32_t neg[4] = {NEG, NEG, NEG, NEG};
 #pragma unroll
     for (int j = 0; j < NPC; ++j)
@@ -278,22 +266,6 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
       if (full || j * PS + lane * EPP < last_nval) {
         cp_async16(dst + j * 512, t + off + j * 512, policy);
         if (d) cp_async16(dst + WB + j * 512, d + off + j * 512, policy);
-      }
-    }
-  };
-
-  // an item past the resident ones, read from global memory into this lane's words: -inf past the
-  // slice end (t: this lane's first byte of the row slice).  Pass 1 reads it keeping it in L2
-  // (evict-last), pass 2 reads it a second time, from L2, letting it go (evict-first).
-  auto glob_words = [&](uint32_t (&W)[NWD], const uint8_t* t, int it, uint64_t pol) {
-    const bool full = it != nitems - 1;
-#pragma unroll
-    for (int j = 0; j < NPC; ++j) {
-      if (full || j * PS + lane * EPP < last_nval) {
-        ldg16(&W[4 * j], t + static_cast<size_t>(it) * IB + j * 512, pol);
-      } else {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) W[4 * j + q] = NEG;
       }
     }
   };
@@ -373,21 +345,15 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
     for (int it = 0; it < nitems; ++it) {
       uint32_t Wt[NWD], Wd[NWD];
       if constexpr (ALIGNED) {
-        if (it < nres) {
-          cp_async_wait_upto(nres - 1 - it);        // this lane's pieces of the item have landed
-          slab_words(Wt, slot(it, 0));
-          if constexpr (PAIR) slab_words(Wd, slot(it, 1));
-        } else {
-          const uint64_t keep = l2_evict_last_policy();
-          glob_words(Wt, A.gt + wl, it, keep);
-          if constexpr (PAIR) glob_words(Wd, A.gd + wl, it, keep);
-        }
+        cp_async_wait_upto(nitems - 1 - it);        // this lane's pieces of the item have landed
+        slab_words(Wt, slot(it, 0));
+        if constexpr (PAIR) slab_words(Wd, slot(it, 1));
       } else {
         row_words(Wt, A.gt, it);
-        if (it < nres) slab_store(slot(it, 0), Wt);
+        slab_store(slot(it, 0), Wt);
         if constexpr (PAIR) {
           row_words(Wd, A.gd, it);
-          if (it < nres) slab_store(slot(it, 1), Wd);
+          slab_store(slot(it, 1), Wd);
         }
       }
       fold(Wt, mt, st);
@@ -395,12 +361,10 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
     }
   };
 
-  // pass 2 of a unit A from the slab (its items past the resident ones from global memory again);
-  // each resident item, once consumed, takes the next unit's copies (nT / nD: this lane's first
-  // byte of its row slices, nT null if there is none).  MODE: alpha only, full masses, or target
-  // masses alone.  Returns the warp's alpha partial (lane-uniform).
-  auto pass2 = [&](auto mode_tag, const SampUnit& A, float offt, float offd, float* mrow, const uint8_t* nT,
-                   const uint8_t* nD) -> float {
+  // pass 2 of a unit from the slab; each item, once consumed, takes the next unit's copies
+  // (nT / nD: this lane's first byte of its row slices, nT null if there is none).  MODE: alpha
+  // only, full masses, or target masses alone.  Returns the warp's alpha partial (lane-uniform).
+  auto pass2 = [&](auto mode_tag, float offt, float offd, float* mrow, const uint8_t* nT, const uint8_t* nD) -> float {
     constexpr int MODE = decltype(mode_tag)::value;
     const uint64_t noff_t = pk(-offt, -offt), noff_d = pk(-offd, -offd);
     const uint64_t neg1 = pk(-1.f, -1.f);
@@ -408,17 +372,8 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
     float pw = 0.f, rw = 0.f;                      // full / single: the warp's totals (lanes 16 / 0)
     for (int it = 0; it < nitems; ++it) {
       uint32_t Wt[NWD], Wd[NWD];
-      if (it < nres) {
-        slab_words(Wt, slot(it, 0));
-        if constexpr (MODE != kModeSingle) slab_words(Wd, slot(it, 1));
-      } else if constexpr (ALIGNED) {
-        const uint64_t drop = l2_evict_first_policy();
-        glob_words(Wt, A.gt + wl, it, drop);
-        if constexpr (MODE != kModeSingle) glob_words(Wd, A.gd + wl, it, drop);
-      } else {
-        row_words(Wt, A.gt, it);
-        if constexpr (MODE != kModeSingle) row_words(Wd, A.gd, it);
-      }
+      slab_words(Wt, slot(it, 0));
+      if constexpr (MODE != kModeSingle) slab_words(Wd, slot(it, 1));
       if constexpr (MODE == kModeAlpha) {
 #pragma unroll
         for (int q = 0; q < NQ; q += 2) {
@@ -461,10 +416,8 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
       }
       if constexpr (ALIGNED) {
         // the item's words are in registers and used: the next unit's copies take its bytes
-        if (it < nres) {
-          if (nT) issue_item(nT, nD, it);
-          cp_async_commit();
-        }
+        if (nT) issue_item(nT, nD, it);
+        cp_async_commit();
       }
     }
     if constexpr (MODE == kModeAlpha) {
@@ -484,7 +437,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
     // the first unit's slice, one commit group per item; pass 2 commits one group per item too,
     // so when pass 1 consumes item it, the groups after it are items it+1 .. nitems-1
     if (hasA)
-      for (int it = 0; it < nres; ++it) {
+      for (int it = 0; it < nitems; ++it) {
         issue_item(A.gt + wl, A.pair ? A.gd + wl : nullptr, it);
         cp_async_commit();
       }
@@ -591,9 +544,9 @@ __global__ void __launch_bounds__(kSampThreads, kSampMinBlocks) sample_kernel(co
     const uint8_t* nD = (hasN && N.pair) ? N.gd + wl : nullptr;
     float* const mrow = P.mass + static_cast<size_t>(A.rec) * kMassRowFloats;
     float aw;
-    if (mode == kModeAlpha) aw = pass2(std::integral_constant<int, kModeAlpha>(), A, offt, offd, mrow, nT, nD);
-    else if (mode == kModeFull) aw = pass2(std::integral_constant<int, kModeFull>(), A, offt, offd, mrow, nT, nD);
-    else aw = pass2(std::integral_constant<int, kModeSingle>(), A, offt, offd, mrow, nT, nD);
+    if (mode == kModeAlpha) aw = pass2(std::integral_constant<int, kModeAlpha>(), offt, offd, mrow, nT, nD);
+    else if (mode == kModeFull) aw = pass2(std::integral_constant<int, kModeFull>(), offt, offd, mrow, nT, nD);
+    else aw = pass2(std::integral_constant<int, kModeSingle>(), offt, offd, mrow, nT, nD);
     prev_aw = aw;
     prev_rec = A.rec;
     has_prev = true;

@@ -109,8 +109,6 @@ struct RowParams {
   int total_units;           // B * U
   int slice;                 // logits per CTA slice (multiple of kChunk)
   int itmax;                 // items of the first (longest) slice
-  int nres;                  // items of each row kept in the slab between the passes (<= itmax);
-                             // later items are read from global memory again in pass 2
   int flags;
   float c;                   // log2(e) / T  (T > 0)
   long long wait_limit;      // ns of wall time per bounded wait; 0 = give up at once

@@ -259,17 +259,8 @@ spec_status_t spec_verify_chain_greedy_static(const void* target_logits, const v
  *                   then waits once more, up to 100 ms, so its copies and
  *                   cluster exchanges still complete before it returns).
  *   cluster         T > 0: CTAs per row of the sampling kernel (1, 2, 4, 8 or
- *                   16); 0: chosen per call shape.  A CTA's slice of a row is
- *                   cut into items of 16 KB: it stays in shared memory
- *                   between the two passes when its items fit (at most 6
- *                   per row); otherwise, for rows on 16-byte boundaries,
- *                   the first item stays and the others are read again, from
- *                   L2, in the second pass.  SPEC_ERR_UNSUPPORTED when
- *                   neither applies, or for more than 80 CTA items per row.
- *   resident_items  T > 0: > 0 keeps at most this many items of each row in
- *                   shared memory and reads the rest twice (rows on 16-byte
- *                   boundaries: 16-byte loads; others: element by element);
- *                   0: as described under cluster.
+ *                   16; a CTA's slice of a row must fit 6 items of 16 KB,
+ *                   else SPEC_ERR_UNSUPPORTED); 0: chosen per call shape.
  *   greedy_variant  T == 0: bit 1 runs the cut in its own kernel instead of
  *                   fusing it into the argmax kernel; bit 2 launches every
  *                   resident CTA slot with the tiles spread evenly.
@@ -290,7 +281,6 @@ typedef struct spec_tuning {
   int greedy_variant;
   int32_t* plan_out;
   void* split_event;
-  int resident_items;
 } spec_tuning_t;
 
 /*

@@ -423,17 +423,14 @@ def _slab_fits(V, esz, cluster):
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("V,cluster", [(24, 16), (4104, 1), (4099, 2), (50008, 4), (128000, 4), (128000, 8),
-                                       (128000, 16), (200003, 1)])
+                                       (128000, 16)])
 def test_slab_sizes(sv, dtype, V, cluster):
     """Every slab size the planner can pick gives the oracle's results: chain, block with a budget,
     and alpha alone (empty CTA slices at V = 24 over 16 CTAs, unaligned rows at V = 4099, ragged
-    last items elsewhere).  A forced cluster size whose slice does not fit streams it when rows are
-    on 16-byte boundaries (the first item of each row stays in shared memory) and is refused
-    otherwise."""
+    last items elsewhere); a forced cluster size whose slice does not fit is refused."""
     esz = 2 if dtype == torch.bfloat16 else 4
-    fits, aligned = _slab_fits(V, esz, cluster), (V * esz) % 16 == 0
     w = W.random_case(seed=V + cluster + esz, B=3, K=4, V=V, T=0.9, dtype=dtype)
-    if not fits and not aligned:
+    if not _slab_fits(V, esz, cluster):
         with pytest.raises(sv.SpecError):
             _run_chain(sv, w, tuning=sv.Tuning(cluster=cluster))
         return
@@ -442,11 +439,8 @@ def test_slab_sizes(sv, dtype, V, cluster):
     compare(_run_chain(sv, w, want_alpha=True, tuning=tun), ref, w)
     assert tun.plan["cluster"] == cluster
     slice_bytes = tun.plan["slice"] * esz
-    if fits:
-        assert 2 * slice_bytes <= tun.plan["smem_bytes"] <= 192 * 1024            # both rows of the slice fit
-        assert tun.plan["smem_bytes"] % (2 * tun.plan["items"]) == 0
-    else:
-        assert tun.plan["smem_bytes"] == 2 * 16384                                # the first item of each row
+    assert 2 * slice_bytes <= tun.plan["smem_bytes"] <= 192 * 1024                # both rows of the slice fit
+    assert tun.plan["smem_bytes"] % (2 * tun.plan["items"]) == 0
     N = 7
     out = _run_block(sv, w, budget=N, tuning=sv.Tuning(cluster=cluster))
     a_ref = oracle_alpha(w)
@@ -463,46 +457,15 @@ def test_slab_sizes(sv, dtype, V, cluster):
     assert sv.default_workspace().status() == 0
 
 
-@pytest.mark.parametrize("dtype,V,cluster,resident", [
-    (torch.bfloat16, 128000, 4, 2), (torch.bfloat16, 128000, 2, 1), (torch.bfloat16, 40003, 1, 2),
-    (torch.float32, 65536, 2, 1), (torch.float32, 30001, 1, 3)])
-def test_streamed_items(sv, dtype, V, cluster, resident):
-    """Slices longer than the slab: the first `resident` items of each row stay in shared memory
-    and the later ones are read from global memory again in pass 2 (rows on and off 16-byte
-    boundaries).  Chain, block with a budget (every row's mass table, the draws from them) and
-    alpha alone give the oracle's results."""
-    esz = 2 if dtype == torch.bfloat16 else 4
-    w = W.random_case(seed=V + 7 * cluster + resident, B=3, K=4, V=V, T=0.9, dtype=dtype)
-    ref = oracle_verify(w)
-    tun = sv.Tuning(cluster=cluster, resident_items=resident)
-    compare(_run_chain(sv, w, want_alpha=True, tuning=tun), ref, w)
-    assert tun.plan["cluster"] == cluster and tun.plan["items"] > resident
-    assert tun.plan["smem_bytes"] == resident * 2 * 16384          # two rows of `resident` 16 KB items
-    assert tun.plan["slice"] * esz > resident * 16384               # the slice is longer than the slab
-    N = 7
-    out = _run_block(sv, w, budget=N, tuning=sv.Tuning(cluster=cluster, resident_items=resident))
-    a_ref = oracle_alpha(w)
-    np.testing.assert_allclose(to_np(out.alpha), a_ref, atol=1e-5, rtol=0)
-    br = O.alloc_budget(a_ref, N)
-    gdepth = out.depth.cpu().numpy()
-    if not check_budget_choice(gdepth, br.conf, N, br.margin):
-        np.testing.assert_array_equal(gdepth, br.depth)
-    compare(out, oracle_verify(w, depth=gdepth), w)
-    t, d, _, _ = _dev(w)
-    a, _, _ = sv.overlap_alpha(t, d, w.temperature, tuning=sv.Tuning(cluster=cluster, resident_items=resident))
-    torch.cuda.synchronize()
-    np.testing.assert_allclose(to_np(a), a_ref, atol=1e-5, rtol=0)
-    assert sv.default_workspace().status() == 0
-
-
 @pytest.mark.parametrize("cluster", [1, 2, 4, 8, 16])
 def test_every_cluster_size_bf16(sv, cluster):
-    """The same bf16 batch at every cluster size gives the oracle's decisions (slices that do not
-    fit in shared memory, at 1 and 2 CTAs per row, are streamed)."""
+    """The same bf16 batch at every cluster size gives the oracle's decisions."""
     w = W.stochastic_mtp(B=6, V=128000)
     ref = oracle_verify(w)
     tun = sv.Tuning(cluster=cluster)
+    if not _slab_fits(128000, 2, cluster):
+        with pytest.raises(sv.SpecError):
+            _run_chain(sv, w, want_alpha=True, tuning=tun)
+        return
     compare(_run_chain(sv, w, want_alpha=True, tuning=tun), ref, w)
     assert tun.plan["cluster"] == cluster
-    assert tun.plan["smem_bytes"] == (2 * 16384 if not _slab_fits(128000, 2, cluster)
-                                      else 2 * 16384 * tun.plan["items"])
