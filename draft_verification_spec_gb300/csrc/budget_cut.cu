@@ -138,13 +138,22 @@ __device__ void sort_desc(float (&v)[E], int n2, int ts, float* xb) {
   }
 }
 
-// Shared scratch of the choice of N: the cost table, scan and reduction slots, the result.
+// Shared scratch of the choice of N: the cost table, scan and reduction slots, the results.
 struct BudgetShared {
   float cn[kBudgetMaxCost], ct[kBudgetMaxCost];
   float run[32], offset[32], best_u[32];
-  int best_n[32];
-  int n;
+  int best_n[32], ties[32], tie_off[32], above[32];
+  int n, above_all, r_last;
 };
+
+__device__ __forceinline__ int warp_incl_scan_int(int v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
 
 // The budget N with the largest expected tokens per unit of verification cost: the first N
 // maximising (B + S(N)) / cost(B + N), S(N) the sum of the N largest prefix confidences, from the
@@ -206,11 +215,23 @@ __device__ int choose_budget(const BudgetParams& P, const float* srt, BudgetShar
   return sh.n;
 }
 
-// The utility / cost choice of N over the [K, B] table `conf`: the confidences sorted (one
-// bitonic sort by the first n2 / E threads), then S(N) and the first maximum of U(N).
+// The last key the budget takes, in its order (c descending, then m ascending, then b ascending,
+// i.e. r = m B + b ascending): key (b, m) is taken when c(b, m) > c_last, or c(b, m) == c_last and
+// m B + b <= r_last.
+struct BudgetCut {
+  float c_last;
+  int r_last;
+};
+
+// The utility / cost choice of N over the [K, B] table `conf`, and the cut of the first N keys:
+// the confidences sorted (one bitonic sort by the first n2 / E threads), S(N) and the first
+// maximum of U(N); c_last is then the N-th largest confidence, and of the ties at c_last the
+// first N - #{c > c_last} in increasing r are taken (one block count and scan).  All keys for
+// N >= B K, none for N = 0.  Writes N to *n_out.
 template <int E>
-__device__ int adaptive_n(const BudgetParams& P, const float* conf, int n2, float* xb, BudgetShared& sh) {
-  const int BK = P.B * P.K, tid = threadIdx.x;
+__device__ BudgetCut adaptive_cut(const BudgetParams& P, const float* conf, int n2, float* xb, BudgetShared& sh,
+                                  int* n_out) {
+  const int BK = P.B * P.K, tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
   const int ts = n2 / E;
   float* const srt = xb + 2 * n2;   // the sorted confidences, descending
   if (tid < ts) {
@@ -225,7 +246,44 @@ __device__ int adaptive_n(const BudgetParams& P, const float* conf, int n2, floa
     for (int e = 0; e < E; ++e) srt[tid * E + e] = v[e];
   }
   __syncthreads();
-  return choose_budget(P, srt, sh);
+  const int N = choose_budget(P, srt, sh);
+  *n_out = N;
+  if (N <= 0) return BudgetCut{2.f, -1};
+  if (N >= BK) return BudgetCut{-1.f, -1};
+  const float cl = srt[N - 1];
+  // each thread counts a contiguous run of positions: above c_last, and ties with it
+  const int per = (BK + nt - 1) / nt;
+  const int r0 = min(BK, tid * per), r1 = min(BK, r0 + per);
+  int above = 0, ties = 0;
+  for (int r = r0; r < r1; ++r) {
+    const float c = conf[r];
+    above += c > cl;
+    ties += c == cl;
+  }
+  const int ties_incl = warp_incl_scan_int(ties, lane);
+  const int above_w = warp_sum_int(above);
+  if (lane == 31) sh.ties[warp] = ties_incl;
+  if (lane == 0) sh.above[warp] = above_w;
+  __syncthreads();
+  if (warp == 0) {
+    const int t = lane < nw ? sh.ties[lane] : 0;
+    const int ti = warp_incl_scan_int(t, lane);
+    if (lane < nw) sh.tie_off[lane] = ti - t;
+    const int a = warp_sum_int(lane < nw ? sh.above[lane] : 0);
+    if (lane == 0) sh.above_all = a;
+  }
+  __syncthreads();
+  const int want = N - sh.above_all;   // ties taken: at least 1, at most the ties there are
+  int seen = sh.tie_off[warp] + ties_incl - ties;
+  if (seen < want && seen + ties >= want) {
+    for (int r = r0; r < r1; ++r)
+      if (conf[r] == cl && ++seen == want) {
+        sh.r_last = r;
+        break;
+      }
+  }
+  __syncthreads();
+  return BudgetCut{cl, sh.r_last};
 }
 
 // Values per sorting thread of the choice of N: n2 / 256 within [1, 16] (at most 256 sorting threads
@@ -313,17 +371,20 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid
     }
   }
   __syncthreads();
+  // with N chosen by utility / cost the keys are sorted anyway, and the cut of the first N comes
+  // from the sorted order; with a given N, each request ranks its own keys (below)
   int Nsel = P.N;
+  BudgetCut cut = {0.f, 0};
   if (P.n_cost > 0) {
     int n2 = 32;
     while (n2 < BK) n2 <<= 1;
     float* const xb = conf + 2 * BK + (BK + 3) / 4;
     switch (budget_values_per_thread(n2)) {
-      case 1: Nsel = adaptive_n<1>(P, conf, n2, xb, sh); break;
-      case 2: Nsel = adaptive_n<2>(P, conf, n2, xb, sh); break;
-      case 4: Nsel = adaptive_n<4>(P, conf, n2, xb, sh); break;
-      case 8: Nsel = adaptive_n<8>(P, conf, n2, xb, sh); break;
-      default: Nsel = adaptive_n<16>(P, conf, n2, xb, sh); break;
+      case 1: cut = adaptive_cut<1>(P, conf, n2, xb, sh, &Nsel); break;
+      case 2: cut = adaptive_cut<2>(P, conf, n2, xb, sh, &Nsel); break;
+      case 4: cut = adaptive_cut<4>(P, conf, n2, xb, sh, &Nsel); break;
+      case 8: cut = adaptive_cut<8>(P, conf, n2, xb, sh, &Nsel); break;
+      default: cut = adaptive_cut<16>(P, conf, n2, xb, sh, &Nsel); break;
     }
     if (blockIdx.x == 0 && threadIdx.x == 0 && P.out_N) *P.out_N = Nsel;
   }
@@ -343,13 +404,22 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_cut_kernel(const __grid
       }
       return warp_sum_int(cnt);
     };
-    // d_b = the number of m whose key ranks below N (a prefix of m)
-    int lo = 0, hi = K;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (rank_of(mid) < Nsel) lo = mid + 1; else hi = mid;
+    int d;
+    if (P.n_cost > 0) {
+      // the positions at or above the cut, a prefix of m (c never grows with m, and among ties
+      // the smaller m comes first)
+      const float cm = lane < K ? conf[lane * B + b] : -1.f;
+      d = __popc(__ballot_sync(0xffffffffu,
+                               lane < K && (cm > cut.c_last || (cm == cut.c_last && lane * B + b <= cut.r_last))));
+    } else {
+      // d_b = the number of m whose key ranks below N (a prefix of m)
+      int lo = 0, hi = K;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (rank_of(mid) < Nsel) lo = mid + 1; else hi = mid;
+      }
+      d = lo;
     }
-    const int d = lo;
     if (P.out_depth && lane == 0) P.out_depth[b] = d;
     if (P.out_conf)
       for (int k = lane; k < K; k += 32) P.out_conf[static_cast<size_t>(b) * K + k] = conf[k * B + b];
