@@ -668,20 +668,32 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     w = make_workload(args.config, 0)
-    # size the per-step sample (whole requests) so the whole run stays within a few minutes
+    # size the per-step sample so the whole run (warm-up included) stays within a few minutes:
+    # whole requests while they fit, else the first m drafted positions of one request (down to
+    # one (target, draft) row pair); a pair stands for its share of the batch's verified tokens
+    budget_s = 150.0
+    per_step = budget_s / max(1, args.steps + args.warmup)
+    pairs_total = max(1, w.B * w.K)
+    tokens_per_pair = verified_tokens(w) / pairs_total
     t0 = time.perf_counter()
     oracle_pass(_subset(w, 1))
     per_req = time.perf_counter() - t0
-    budget_s = 150.0
-    n_req = int(max(1, min(w.B, budget_s / max(1, args.steps + args.warmup) / max(per_req, 1e-6))))
-    sub = _subset(w, n_req)
+    if per_req <= per_step or w.K == 0:
+        n_req = int(max(1, min(w.B, per_step / max(per_req, 1e-6))))
+        sub, pairs, what = _subset(w, n_req), n_req * max(1, w.K), f"{n_req} request(s) of the {w.B}-request batch"
+    else:
+        t0 = time.perf_counter()
+        oracle_pass(_prefix(w, 1))
+        per_pair = time.perf_counter() - t0
+        m = int(max(1, min(w.K, per_step / max(per_pair, 1e-6))))
+        sub, pairs, what = _prefix(w, m), m, f"the first {m} of {w.K} drafted position(s) of one request"
     for _ in range(args.warmup):
-        oracle_pass(_subset(w, 1))
+        oracle_pass(sub)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         oracle_pass(sub)
     dt = time.perf_counter() - t0
-    value = args.steps * verified_tokens(sub) / dt
+    value = args.steps * pairs * tokens_per_pair / dt
     cores = _threads_used()
     return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
@@ -690,11 +702,18 @@ def run_reference(args, rank, world):
             "config": {"workload": f"{args.config} B={w.B} K={w.K} V={w.V} T={w.temperature}"
                                    + (f" N={w.budget}" if w.budget is not None else "")},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"{n_req} request(s) of the {w.B}-request batch per step "
-                                       f"(budget scaled to {sub.budget})" if w.budget is not None else
-                                       f"{n_req} request(s) of the {w.B}-request batch per step",
+                             "sample": f"{what} per step ({tokens_per_pair:g} verified token(s) per "
+                                       f"drafted position, the batch's share)",
                              "cpu": _cpu_model()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def _prefix(w, m):
+    """Request 0 of a workload cut to its first m drafted positions (its budget scaled to them)."""
+    import workloads as W
+    b = None if w.budget is None else max(1, w.budget * m // max(1, w.B * w.K))
+    return W.Workload(w.name, w.target[:1, :m + 1], w.draft[:1, :m], w.tokens[:1, :m], w.uniforms[:1, :m + 1],
+                      w.temperature, b, w.meta)
 
 
 def _subset(w, n):
@@ -709,7 +728,7 @@ def _subset(w, n):
 def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=60000)
+    ap.add_argument("--steps", type=int, default=6000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="budget_sweep_B64")
