@@ -82,7 +82,19 @@ def test_reference_arm_budgeted_config_scales_the_budget():
         bench.main(["--impl", "reference", "--config", "budget_sweep_B4", "--steps", "3", "--warmup", "3"])
     d = json.loads([ln for ln in buf.getvalue().splitlines() if ln.startswith("{")][0])
     assert d["impl"] == "reference" and d["value"] > 0
-    assert "N=32" in d["config"]["workload"] and "budget scaled" in d["cpu_baseline"]["sample"]
+    assert "N=32" in d["config"]["workload"] and "the batch's share" in d["cpu_baseline"]["sample"]
+    assert "0.5 verified token(s) per drafted position" in d["cpu_baseline"]["sample"]   # N / (B K) = 32 / 64
+
+
+def test_reference_arm_prefix_sample():
+    """A request cut to its first m drafted positions keeps the rows those positions need, and its
+    budget is the batch's scaled to them."""
+    w = W.budget_sweep(4, V=1000)
+    p = bench._prefix(w, 3)
+    assert (p.B, p.K, p.V) == (1, 3, 1000)
+    assert tuple(p.target.shape) == (1, 4, 1000) and tuple(p.uniforms.shape) == (1, 4)
+    assert p.budget == max(1, w.budget * 3 // (w.B * w.K))
+    assert bool((p.target[0] == w.target[0, :4]).all()) and bool((p.tokens[0] == w.tokens[0, :3]).all())
 
 
 def test_verified_tokens_is_the_budget_when_there_is_one():
