@@ -12,6 +12,7 @@
 #include <vector>
 
 #include "../../include/spec_verify.h"
+#include "api_range.h"
 #include "spec_internal.h"
 
 namespace sv {
@@ -558,6 +559,7 @@ size_t spec_workspace_bytes(int B, int K, int V, int dtype) {
 }
 
 spec_status_t spec_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
+  const sv::ApiRange range("spec_workspace_init");
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0) return SPEC_ERR_WORKSPACE;
   return cudaMemsetAsync(workspace, 0, ws_bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? SPEC_OK
@@ -565,6 +567,7 @@ spec_status_t spec_workspace_init(void* workspace, size_t ws_bytes, void* stream
 }
 
 spec_status_t spec_get_status(void* workspace, void* stream, int32_t* out_status) {
+  const sv::ApiRange range("spec_get_status");
   if (!workspace || !out_status) return SPEC_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t h = 0;
@@ -582,6 +585,7 @@ spec_status_t spec_verify_chain(const void* target_logits, const void* draft_log
                                 float temperature, const int32_t* depth, int32_t* out_tokens,
                                 int32_t* out_accepted, float* out_alpha, void* workspace,
                                 size_t ws_bytes, void* stream) {
+  const sv::ApiRange range("spec_verify_chain");
   VerifyArgs a = {target_logits, draft_logits, dtype, tokens, uniforms, B, K, V, temperature,
                   depth, -1, out_tokens, out_accepted, out_alpha, nullptr, nullptr, nullptr,
                   workspace, ws_bytes, static_cast<cudaStream_t>(stream)};
@@ -594,6 +598,7 @@ spec_status_t spec_verify_block(const void* target_logits, const void* draft_log
                                 int32_t* out_tokens, int32_t* out_accepted, float* out_alpha,
                                 float* out_cum_alpha, float* out_expected_len, int32_t* out_depth,
                                 void* workspace, size_t ws_bytes, void* stream) {
+  const sv::ApiRange range("spec_verify_block");
   VerifyArgs a = {target_logits, draft_logits, dtype, tokens, uniforms, B, K, V, temperature,
                   depth, budget_N, out_tokens, out_accepted, out_alpha, out_cum_alpha,
                   out_expected_len, out_depth, workspace, ws_bytes, static_cast<cudaStream_t>(stream)};
@@ -604,6 +609,7 @@ spec_status_t spec_overlap_alpha(const void* target_logits, const void* draft_lo
                                  int B, int K, int V, float temperature, float* out_alpha,
                                  float* out_cum_alpha, float* out_expected_len, void* workspace,
                                  size_t ws_bytes, void* stream) {
+  const sv::ApiRange range("spec_overlap_alpha");
   return run_overlap(target_logits, draft_logits, dtype, B, K, V, temperature, out_alpha, out_cum_alpha,
                      out_expected_len, workspace, ws_bytes, static_cast<cudaStream_t>(stream), Knobs());
 }
@@ -614,6 +620,7 @@ spec_status_t spec_verify_tuned(const void* target_logits, const void* draft_log
                                 int32_t* out_tokens, int32_t* out_accepted, float* out_alpha,
                                 float* out_cum_alpha, float* out_expected_len, int32_t* out_depth,
                                 void* workspace, size_t ws_bytes, void* stream, const spec_tuning_t* tuning) {
+  const sv::ApiRange range("spec_verify_tuned");
   const Knobs kn = knobs_of(tuning);
   if (tuning && tuning->cluster != 0) {
     const int c = tuning->cluster;
@@ -630,6 +637,7 @@ spec_status_t spec_verify_tuned(const void* target_logits, const void* draft_log
 
 spec_status_t spec_alloc_budget(const float* alpha, int B, int K, int budget_N, int32_t* out_depth,
                                 float* out_conf, void* workspace, size_t ws_bytes, void* stream) {
+  const sv::ApiRange range("spec_alloc_budget");
   if (B < 0 || K < 0 || budget_N < 0) return SPEC_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * K > kBudgetMaxKeys) return SPEC_ERR_UNSUPPORTED;
   if (B == 0) return SPEC_OK;
@@ -653,6 +661,7 @@ spec_status_t spec_alloc_budget(const float* alpha, int B, int K, int budget_N, 
 spec_status_t spec_alloc_budget_adaptive(const float* alpha, int B, int K, const float* cost_n,
                                          const float* cost_t, int n_cost, int32_t* out_N, int32_t* out_depth,
                                          float* out_conf, void* workspace, size_t ws_bytes, void* stream) {
+  const sv::ApiRange range("spec_alloc_budget_adaptive");
   if (B < 0 || K < 0 || n_cost < 1) return SPEC_ERR_INVALID_ARG;
   if (n_cost > sv::kBudgetMaxCost) return SPEC_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * K > kBudgetMaxKeys) return SPEC_ERR_UNSUPPORTED;
@@ -680,6 +689,7 @@ spec_status_t spec_draft_budget(const void* draft_logits, int dtype, const int32
                                 float temperature, int budget_N, const float* cost_n, const float* cost_t,
                                 int n_cost, int32_t* out_N, int32_t* out_depth, float* out_conf,
                                 void* workspace, size_t ws_bytes, void* stream) {
+  const sv::ApiRange range("spec_draft_budget");
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
   if (B < 0 || K < 0 || V < 1 || bad_T(temperature) || n_cost < 0) return SPEC_ERR_INVALID_ARG;
   if (n_cost == 0 && budget_N < 0) return SPEC_ERR_INVALID_ARG;

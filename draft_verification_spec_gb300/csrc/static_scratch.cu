@@ -8,6 +8,7 @@
 // slots, per-request completion counters) in one file-scope device array of fixed size that
 // every GPU loading the library holds until the process exits.
 #include "../../include/spec_verify.h"
+#include "api_range.h"
 #include "spec_internal.h"
 
 namespace {
@@ -42,6 +43,7 @@ extern "C" spec_status_t spec_verify_chain_greedy_static(const void* target_logi
                                                          const int32_t* depth, int32_t* out_tokens,
                                                          int32_t* out_accepted, float* out_alpha,
                                                          int32_t* out_status, void* stream) {
+  const sv::ApiRange range("spec_verify_chain_greedy_static");
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
   if (B < 0 || K < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
   if (K > sv::kMaxK || V > 262144) return SPEC_ERR_UNSUPPORTED;
