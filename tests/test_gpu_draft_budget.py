@@ -160,3 +160,27 @@ def test_draft_budget_degenerate_and_invalid(sv):
         sv.draft_budget(zd, x, 0.7, cost=(list(range(65)), [1.0] * 65))
     with pytest.raises(ValueError):
         sv.draft_budget(zd, x, 0.7)
+
+
+@pytest.mark.parametrize("B,K", [(100, 21), (256, 16), (512, 16), (273, 30)])
+def test_budget_large_batches(sv, B, K):
+    """Up to the documented B K <= 8192 keys (the sort's 8 and 16 values per thread, padding to a
+    power of two, shared memory past 48 KB): the utility / cost N and a given N against the
+    oracle, on dyadic alphas whose products are exact in float32 and tie often."""
+    rng = np.random.default_rng(B * 100 + K)
+    alpha = rng.choice([0.5, 0.75, 1.0, 0.875, 0.25], size=(B, K)).astype(np.float32)
+    d = torch.device("cuda")
+    a32 = torch.tensor(alpha, device=d)
+    a64 = alpha.astype(np.float64)
+    for cost in (W.verify_cost_table(B, K), ([float(B), float(B * (K + 1))], [1.0, 3.0])):
+        n, depth, conf = sv.alloc_budget_adaptive(a32, cost)
+        torch.cuda.synchronize()
+        ref = O.adaptive_budget(a64, *cost)
+        _check_n(int(n.item()), ref)
+        br = O.alloc_budget(a64, int(n.item()))
+        if not check_budget_choice(depth.cpu().numpy(), br.conf, int(n.item()), br.margin):
+            np.testing.assert_array_equal(depth.cpu().numpy(), br.depth)
+    for N in (1, B * K // 3, B * K - 1):
+        depth, _ = sv.alloc_budget(a32, N)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(depth.cpu().numpy(), O.alloc_budget(a64, N).depth)
